@@ -1,0 +1,571 @@
+// gemm.cu -- block-scaled W4A4 GEMMs on the sm_103a tensor cores (tcgen05).
+//
+//   Y[m, n] = bf16_rn( S_a[m] * S_b[n] * sum_k dec(a)[m, k] * dec(b)[n, k] )
+//
+// dec(.) = E4M3 block scale x E2M1 value; the block scales are applied by the
+// tensor core itself (tcgen05.mma kind::mxf4nvf4, block_scale, 4 scales per
+// 64-element K step) and the per-token / per-row FP32 scales in the epilogue, in
+// the same kernel ("Towards Blackwell-Native 8-bit and 4-bit RL", results item
+// 10: applying the per-token scale as a separate op is what made the unfused
+// path slower than BF16; "TRIAGE", section "NVFP4 quantization format and W4A4
+// execution": W4A4 runs natively on the tensor cores).
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0      TMA producer: A/B tiles (cp.async.bulk.tensor, 128B swizzle) and
+//               the swizzled scale tiles (cp.async.bulk) into a 4-stage ring.
+//   warp 1      TMEM allocator + MMA issuer: tcgen05.cp moves the scale tiles
+//               from shared memory to TMEM, tcgen05.mma accumulates the 128 x 256
+//               output tile in TMEM, tcgen05.commit releases ring stages.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator, scale by S_a * S_b,
+//               round to bf16, release the accumulator, store.
+// Tile 128 x 256 x 256 (K step of 256 FP4 = 128 bytes = one swizzle row).
+// The grouped (MoE) variant walks the padded per-expert layout: each 128-row
+// tile belongs to one expert, found from the device-side offsets.
+//
+// Every wait is bounded: a wait that runs out sets the status word and a shared
+// abort flag, every role leaves its loop, the producer waits (bounded) for its
+// copies in flight, the MMA thread for its tensor-core work, and TMEM is freed.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBKBytes = 128;                // 256 FP4 values per K step
+constexpr int kStages = 4;
+constexpr int kMmaPerStage = 4;              // K = 64 per tcgen05.mma
+constexpr int kThreads = 192;
+constexpr uint32_t kATileBytes = kBM * kBKBytes;      // 16 KB
+constexpr uint32_t kBTileBytes = kBN * kBKBytes;      // 32 KB
+constexpr uint32_t kSFAtomBytes = 512;                // 128 rows x 4 scales
+constexpr uint32_t kSFATileBytes = 4 * kSFAtomBytes;  // 2 KB per stage
+constexpr uint32_t kSFBTileBytes = 8 * kSFAtomBytes;  // 4 KB per stage
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSFTmemCol = 256;                  // after the 256 accumulator columns
+constexpr uint32_t kSFTmemPerStage = 48;              // 16 (A) + 32 (B)
+constexpr size_t kSmemBytes =
+    1024 + kStages * (kATileBytes + kBTileBytes + kSFATileBytes + kSFBTileBytes) + 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
+constexpr uint64_t kDrainLimitNs = 200000000ull;      // 0.2 s
+
+// Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), K-major,
+// N = 256 (N >> 3 at bit 17), M = 128 (M >> 4 at bit 24), scales UE4M3 (bit 23
+// clear), scale-factor ids 0, dense.
+constexpr uint32_t kInstrDesc = (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) | ((kBM >> 4) << 24);
+
+struct GemmParams {
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    const float* sa;
+    const float* sb;
+    uint16_t* y;
+    const int32_t* offsets;   // grouped only
+    unsigned* status;
+    int64_t M;                // rows of A (dense) or rows capacity (grouped)
+    int64_t N;
+    int64_t ld_y;
+    int64_t sfb_expert_bytes; // grouped: bytes of one expert's scale block
+    int kgroups;              // K / 64: scale words per row
+    int num_k_tiles;
+    int num_n_tiles;
+    int num_m_tiles;          // dense: ceil(M / 128); grouped: capacity tiles
+    int E;                    // grouped: experts; dense: 0
+};
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0),
+          "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+    const uint64_t addr = smem_u32(p);
+    return ((addr >> 4) & 0x3FFFull) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// Descriptor of one 512-byte scale atom (32 rows of 16 bytes, no swizzle,
+// 8-row core matrices 128 bytes apart) for tcgen05.cp.
+__device__ __forceinline__ uint64_t sf_desc(const void* p) {
+    const uint64_t addr = smem_u32(p);
+    return ((addr >> 4) & 0x3FFFull) | ((128ull >> 4) << 32) | (1ull << 46);
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate, uint32_t sfa_tmem, uint32_t sfb_tmem) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kInstrDesc), "r"(accumulate), "r"(sfa_tmem),
+          "r"(sfb_tmem)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns; thread t gets lane (base + t).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    // The wait names the registers so no use of them can move above it.
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+          "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+          "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+          "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+          "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+        :: "memory");
+}
+
+// ----------------------------------------------------------------------------
+// Tile schedule (identical in every role)
+// ----------------------------------------------------------------------------
+struct Tile {
+    int64_t m0;        // first row of A / Y
+    int64_t n0;        // first column of Y (row of B inside the expert)
+    int64_t b_row0;    // first row of B in the stacked [E * N] weights
+    int m_tile;        // row tile of A's scales
+    int expert;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ int num_tiles(const GemmParams& p, int used_m_tiles) {
+    return (kGrouped ? used_m_tiles : p.num_m_tiles) * p.num_n_tiles;
+}
+
+template <bool kGrouped>
+__device__ __forceinline__ Tile tile_at(const GemmParams& p, int t, int used_m_tiles) {
+    Tile tl;
+    const int mt_count = kGrouped ? used_m_tiles : p.num_m_tiles;
+    tl.m_tile = t % mt_count;
+    const int nt = t / mt_count;
+    tl.m0 = static_cast<int64_t>(tl.m_tile) * kBM;
+    tl.n0 = static_cast<int64_t>(nt) * kBN;
+    tl.expert = 0;
+    if (kGrouped) {
+        // expert e with offsets[e] <= m0 < offsets[e + 1]
+        int lo = 0, hi = p.E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<int64_t>(__ldg(p.offsets + mid)) <= tl.m0) lo = mid;
+            else hi = mid - 1;
+        }
+        tl.expert = lo;
+    }
+    tl.b_row0 = static_cast<int64_t>(tl.expert) * p.N + tl.n0;
+    return tl;
+}
+
+template <bool kGrouped>
+__global__ void __launch_bounds__(kThreads, 1)
+    nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                      const __grid_constant__ CUtensorMap tma_b, GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + kStages * kATileBytes;
+    uint8_t* sSFA = sB + kStages * kBTileBytes;
+    uint8_t* sSFB = sSFA + kStages * kSFATileBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBTileBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* acc_full = empty + kStages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain = acc_empty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Rows in use (grouped): the padded layout ends at offsets[E].
+    int used_m_tiles = p.num_m_tiles;
+    if (kGrouped) {
+        int64_t used = __ldg(p.offsets + p.E);
+        if (used > p.M || used < 0) {
+            if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
+            used = used < 0 ? 0 : p.M;
+        }
+        used_m_tiles = static_cast<int>((used + kBM - 1) / kBM);
+    }
+    const int tiles = num_tiles<kGrouped>(p, used_m_tiles);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4 * 32);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_holder)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------ producer ------------------------------
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_b)) : "memory");
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued_mask = 0, last_phase = 0;
+        bool ok = true;
+        const int sfb_tiles_n = static_cast<int>((p.N + 127) / 128);
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            const Tile tl = tile_at<kGrouped>(p, t, used_m_tiles);
+            if (kGrouped && (__ldg(p.offsets + tl.expert) & (kBM - 1)) != 0)
+                record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
+            const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
+            const int nt128 = static_cast<int>(tl.n0 / 128);
+            const bool two_b_atoms = nt128 + 1 < sfb_tiles_n;
+            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                const uint32_t sf_bytes = ng * kSFAtomBytes;
+                const uint32_t bytes =
+                    kATileBytes + kBTileBytes + sf_bytes + (two_b_atoms ? 2 : 1) * sf_bytes;
+                mbar_arrive_expect_tx(&full[stage], bytes);
+                tma_load_2d(&tma_a, &full[stage], sA + stage * kATileBytes, kt * kBKBytes,
+                            static_cast<int32_t>(tl.m0));
+                tma_load_2d(&tma_b, &full[stage], sB + stage * kBTileBytes, kt * kBKBytes,
+                            static_cast<int32_t>(tl.b_row0));
+                const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
+                bulk_load(sSFA + stage * kSFATileBytes,
+                          p.sfa + (static_cast<int64_t>(tl.m_tile) * p.kgroups + g0) * kSFAtomBytes,
+                          sf_bytes, &full[stage]);
+                bulk_load(sSFB + stage * kSFBTileBytes,
+                          sfb_e + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes,
+                          sf_bytes, &full[stage]);
+                if (two_b_atoms)
+                    bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
+                              sfb_e + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
+                              sf_bytes, &full[stage]);
+                issued_mask |= 1u << stage;
+                last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
+        }
+        // every copy this thread issued must land before the CTA may exit
+        for (int s = 0; s < kStages; ++s)
+            if (issued_mask & (1u << s))
+                if (!mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kDrainLimitNs, nullptr))
+                    record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------ MMA issuer ----------------------------
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                const uint32_t sf_col = tmem + kSFTmemCol + stage * kSFTmemPerStage;
+                const uint8_t* sfa_s = sSFA + stage * kSFATileBytes;
+                const uint8_t* sfb_s = sSFB + stage * kSFBTileBytes;
+                for (int j = 0; j < ng; ++j) {
+                    tc_cp_sf(sf_col + j * 4, sf_desc(sfa_s + j * kSFAtomBytes));
+                    tc_cp_sf(sf_col + 16 + j * 8, sf_desc(sfb_s + j * kSFAtomBytes));
+                    tc_cp_sf(sf_col + 16 + j * 8 + 4, sf_desc(sfb_s + kSFATileBytes + j * kSFAtomBytes));
+                }
+                const uint8_t* a_s = sA + stage * kATileBytes;
+                const uint8_t* b_s = sB + stage * kBTileBytes;
+                for (int j = 0; j < ng; ++j) {
+                    tc_mma(tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32),
+                           (kt > 0 || j > 0) ? 1u : 0u, sf_col + j * 4, sf_col + 16 + j * 8);
+                }
+                tc_commit(&empty[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            tc_commit(acc_full);
+            acc_phase ^= 1u;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
+        }
+        // all tensor-core work issued by this thread completes before TMEM is freed
+        tc_commit(drain);
+        if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr))
+            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
+    } else if (warp >= 2) {
+        // ------------------------------ epilogue ------------------------------
+        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            bool ok = mbar_wait_bounded(acc_full, acc_phase, kWaitLimitNs, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                *abort_flag = 1;
+                if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const Tile tl = tile_at<kGrouped>(p, t, used_m_tiles);
+            const int64_t m = tl.m0 + quad * 32 + lane;
+            const float sa = (m < p.M) ? __ldg(p.sa + m) : 0.0f;
+            const float* sbp = p.sb + (kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + tl.n0;
+            uint32_t packed[kBN / 2];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_row + c * 32, r);
+                const int64_t ncol = tl.n0 + c * 32 + lane;
+                const float sbv = (ncol < p.N) ? __ldg(sbp + c * 32 + lane) : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const float s0 = __fmul_rn(sa, __shfl_sync(0xFFFFFFFFu, sbv, j));
+                    const float s1 = __fmul_rn(sa, __shfl_sync(0xFFFFFFFFu, sbv, j + 1));
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(
+                        __fmul_rn(__uint_as_float(r[j]), s0), __fmul_rn(__uint_as_float(r[j + 1]), s1));
+                    packed[c * 16 + j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+            acc_phase ^= 1u;
+            if (m < p.M) {
+                uint16_t* yrow = p.y + m * p.ld_y + tl.n0;
+#pragma unroll
+                for (int v = 0; v < kBN / 8; ++v) {
+                    if (tl.n0 + v * 8 < p.N)
+                        reinterpret_cast<uint4*>(yrow)[v] =
+                            make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                       packed[4 * v + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols) : "memory");
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+// Rows of `row_bytes` packed bytes; box = 128 bytes x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kGrouped>
+nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
+                         int tiles_upper, const DeviceCtx& ctx, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    if (!attr_set[ctx.device & 63]) {
+        if (cudaFuncSetAttribute(nvfp4_gemm_kernel<kGrouped>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        attr_set[ctx.device & 63] = true;
+    }
+    const int grid = tiles_upper < ctx.sm_count ? tiles_upper : ctx.sm_count;
+    if (grid <= 0) return NVFP4_OK;
+    nvfp4_gemm_kernel<kGrouped><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
+}
+
+nvfp4_status check_operand_shapes(int64_t N, int64_t K) {
+    if (N <= 0 || N % 16 != 0 || K <= 0 || K % 64 != 0) return NVFP4_ERR_SHAPE;
+    if (K > (int64_t(1) << 20) || N > (int64_t(1) << 24)) return NVFP4_ERR_SHAPE;
+    return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int64_t M,
+                        const void* b_q, const void* b_sf, const float* b_s, int64_t N, int64_t K,
+                        void* y, int64_t ld_y, nvfp4_stream_t stream) {
+    DeviceCtx ctx;
+    nvfp4_status st = device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
+    if (M < 0 || M > (int64_t(1) << 31) - kBM) return NVFP4_ERR_SHAPE;
+    if ((st = check_operand_shapes(N, K)) != NVFP4_OK) return st;
+    if (ld_y < N || ld_y % 8 != 0) return NVFP4_ERR_SHAPE;
+    if (M == 0) return NVFP4_OK;
+    if (!a_q || !a_sf || !a_s || !b_q || !b_sf || !b_s || !y) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(a_q, 16) || !aligned(b_q, 16) || !aligned(a_sf, 16) || !aligned(b_sf, 16) ||
+        !aligned(y, 16) || !aligned(a_s, 4) || !aligned(b_s, 4))
+        return NVFP4_ERR_ALIGNMENT;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a_q, M, K / 2, kBM) || !make_map(&mb, b_q, N, K / 2, kBN)) return NVFP4_ERR_CUDA;
+    GemmParams p;
+    p.sfa = static_cast<const uint8_t*>(a_sf);
+    p.sfb = static_cast<const uint8_t*>(b_sf);
+    p.sa = a_s;
+    p.sb = b_s;
+    p.y = static_cast<uint16_t*>(y);
+    p.offsets = nullptr;
+    p.status = ctx.status;
+    p.M = M;
+    p.N = N;
+    p.ld_y = ld_y;
+    p.sfb_expert_bytes = 0;
+    p.kgroups = static_cast<int>(K / 64);
+    p.num_k_tiles = static_cast<int>(ceil_div(K, 256));
+    p.num_n_tiles = static_cast<int>(ceil_div(N, kBN));
+    p.num_m_tiles = static_cast<int>(ceil_div(M, kBM));
+    p.E = 0;
+    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+    if (tiles > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
+    return launch_gemm<false>(ma, mb, p, static_cast<int>(tiles), ctx,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* a_s,
+                                int64_t rows_capacity, const int32_t* expert_offsets, int32_t E,
+                                const void* b_q, const void* b_sf, const float* b_s, int64_t N,
+                                int64_t K, void* y, nvfp4_stream_t stream) {
+    DeviceCtx ctx;
+    nvfp4_status st = device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
+    if (rows_capacity < 0 || rows_capacity > (int64_t(1) << 31) - kBM) return NVFP4_ERR_SHAPE;
+    if (E < 1 || E > 1024) return NVFP4_ERR_SHAPE;
+    if ((st = check_operand_shapes(N, K)) != NVFP4_OK) return st;
+    if (rows_capacity == 0) return NVFP4_OK;
+    if (!a_q || !a_sf || !a_s || !expert_offsets || !b_q || !b_sf || !b_s || !y)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(a_q, 16) || !aligned(b_q, 16) || !aligned(a_sf, 16) || !aligned(b_sf, 16) ||
+        !aligned(y, 16) || !aligned(a_s, 4) || !aligned(b_s, 4) || !aligned(expert_offsets, 4))
+        return NVFP4_ERR_ALIGNMENT;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a_q, rows_capacity, K / 2, kBM) ||
+        !make_map(&mb, b_q, static_cast<int64_t>(E) * N, K / 2, kBN))
+        return NVFP4_ERR_CUDA;
+    GemmParams p;
+    p.sfa = static_cast<const uint8_t*>(a_sf);
+    p.sfb = static_cast<const uint8_t*>(b_sf);
+    p.sa = a_s;
+    p.sb = b_s;
+    p.y = static_cast<uint16_t*>(y);
+    p.offsets = expert_offsets;
+    p.status = ctx.status;
+    p.M = rows_capacity;
+    p.N = N;
+    p.ld_y = N;
+    p.sfb_expert_bytes = static_cast<int64_t>(nvfp4_sf_bytes(N, K));
+    p.kgroups = static_cast<int>(K / 64);
+    p.num_k_tiles = static_cast<int>(ceil_div(K, 256));
+    p.num_n_tiles = static_cast<int>(ceil_div(N, kBN));
+    p.num_m_tiles = static_cast<int>(ceil_div(rows_capacity, kBM));
+    p.E = E;
+    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+    if (tiles > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
+    return launch_gemm<true>(ma, mb, p, static_cast<int>(tiles), ctx,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+// permute.cu -- MoE routing permute into a contiguous, padded per-expert layout.
+//
+// Counting sort over the flattened (token, slot) pairs, stable in (token, slot)
+// order, with all metadata left on the device ("miniTE report", section
+// "Transformer Engine path optimisation": contiguous layouts and device-side
+// metadata feed the grouped GEMM without a host round trip).
+//   1. count:   one block per chunk of kChunk pairs -> per-chunk expert histogram
+//   2. scan:    one block: per-expert totals, padded exclusive scan -> offsets,
+//               and each chunk's first row inside each expert segment
+//   3. scatter: one block per chunk, in order: rank inside the chunk from
+//               warp match + per-warp histograms -> gather_rows / dst_rows
+#include "common.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kChunk = 1024;
+constexpr int kPermThreads = 256;
+constexpr int kMaxExperts = 1024;
+
+__global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t* ids, int64_t n,
+                                                                  int E, int32_t* counts,
+                                                                  unsigned* status) {
+    extern __shared__ int32_t s_hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    __syncthreads();
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int64_t c1 = min(c0 + kChunk, n);
+    for (int64_t i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
+        const int32_t e = ids[i];
+        if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
+        else record_error(status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_ID);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        counts[static_cast<int64_t>(blockIdx.x) * E + e] = s_hist[e];
+}
+
+// One block of round_up(E, 32) threads (<= 1024).
+__global__ void perm_scan_kernel(int32_t* counts, int nchunks, int E, int align, int32_t* offsets) {
+    __shared__ int32_t s_warp[32];
+    const int e = threadIdx.x;
+    const int lane = e & 31, warp = e >> 5;
+    int64_t total = 0;
+    if (e < E)
+        for (int c = 0; c < nchunks; ++c) total += counts[static_cast<int64_t>(c) * E + e];
+    const int32_t padded = static_cast<int32_t>((total + align - 1) / align * align);
+    // block-wide exclusive scan of the padded segment lengths
+    int32_t incl = padded;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int32_t w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += t;
+        }
+        if (lane < nw) s_warp[lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    const int32_t excl = incl - padded + (warp > 0 ? s_warp[warp - 1] : 0);
+    if (e < E) {
+        offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + padded;
+        int32_t base = excl;
+        for (int c = 0; c < nchunks; ++c) {
+            const int64_t idx = static_cast<int64_t>(c) * E + e;
+            const int32_t cnt = counts[idx];
+            counts[idx] = base;
+            base += cnt;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_t* ids, int64_t n,
+                                                                    int topk, int E,
+                                                                    const int32_t* chunk_base,
+                                                                    int32_t* gather,
+                                                                    int32_t* dst_rows) {
+    extern __shared__ int32_t smem[];
+    int32_t* s_next = smem;                 // [E] next free row of each expert for this chunk
+    int32_t* s_wcnt = smem + E;             // [kPermThreads/32][E] pairs per warp this round
+    constexpr int kWarps = kPermThreads / 32;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        s_next[e] = chunk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+        for (int w = 0; w < kWarps; ++w) s_wcnt[w * E + e] = 0;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int64_t c1 = min(c0 + kChunk, n);
+    for (int64_t base = c0; base < c1; base += kPermThreads) {
+        const int64_t i = base + threadIdx.x;
+        int32_t e = (i < c1) ? ids[i] : -1;
+        if (e >= E) e = -1;
+        if (i < c1 && e < 0) dst_rows[i] = -1;   // dropped id (already reported by the count pass)
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        if (e >= 0 && lower == 0u) s_wcnt[warp * E + e] = __popc(peers);
+        __syncthreads();
+        if (e >= 0) {
+            int32_t row = s_next[e] + __popc(lower);
+            for (int w = 0; w < warp; ++w) row += s_wcnt[w * E + e];
+            gather[row] = static_cast<int32_t>(i / topk);
+            dst_rows[i] = row;
+        }
+        __syncthreads();
+        for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
+            int32_t add = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                add += s_wcnt[w * E + ee];
+                s_wcnt[w * E + ee] = 0;
+            }
+            s_next[ee] += add;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+int64_t nvfp4_moe_capacity(int64_t tokens, int32_t topk, int32_t num_experts, int32_t row_align) {
+    if (tokens < 0 || topk <= 0 || num_experts <= 0 || row_align <= 0) return 0;
+    return round_up(tokens * topk + static_cast<int64_t>(num_experts) * (row_align - 1), row_align);
+}
+
+size_t nvfp4_moe_permute_workspace_bytes(int64_t tokens, int32_t topk, int32_t num_experts) {
+    if (tokens < 0 || topk <= 0 || num_experts <= 0) return 0;
+    const int64_t chunks = ceil_div(tokens * topk, kChunk);
+    const int64_t bytes = chunks * num_experts * 4;
+    return static_cast<size_t>(bytes < 256 ? 256 : bytes);
+}
+
+nvfp4_status nvfp4_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t topk,
+                               int32_t num_experts, int32_t row_align, int32_t* expert_offsets,
+                               int32_t* gather_rows, int64_t capacity, int32_t* dst_rows,
+                               void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    DeviceCtx ctx;
+    nvfp4_status st = device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
+    if (tokens < 0 || topk < 1 || topk > 64 || num_experts < 1 || num_experts > kMaxExperts ||
+        row_align < 1)
+        return NVFP4_ERR_SHAPE;
+    const int64_t n = tokens * topk;
+    if (n > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
+    if (capacity < nvfp4_moe_capacity(tokens, topk, num_experts, row_align)) return NVFP4_ERR_SHAPE;
+    if (capacity > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
+    if (expert_offsets == nullptr || gather_rows == nullptr || (n > 0 && (topk_ids == nullptr || dst_rows == nullptr)))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(topk_ids, 4) || !aligned(expert_offsets, 4) || !aligned(gather_rows, 4) ||
+        !aligned(dst_rows, 4) || !aligned(workspace, 4))
+        return NVFP4_ERR_ALIGNMENT;
+    if (workspace == nullptr ||
+        workspace_bytes < nvfp4_moe_permute_workspace_bytes(tokens, topk, num_experts))
+        return NVFP4_ERR_WORKSPACE;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t* counts = static_cast<int32_t*>(workspace);
+    const int nchunks = static_cast<int>(ceil_div(n, kChunk));
+    const int E = num_experts;
+    if (cudaMemsetAsync(gather_rows, 0xFF, static_cast<size_t>(capacity) * 4, s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (nchunks > 0) {
+        perm_count_kernel<<<nchunks, kPermThreads, E * sizeof(int32_t), s>>>(topk_ids, n, E, counts,
+                                                                               ctx.status);
+        NVFP4_CHECK_LAUNCH();
+    }
+    perm_scan_kernel<<<1, static_cast<unsigned>(round_up(E, 32)), 0, s>>>(counts, nchunks, E,
+                                                                          row_align, expert_offsets);
+    NVFP4_CHECK_LAUNCH();
+    if (nchunks > 0) {
+        const size_t smem = static_cast<size_t>(E) * (1 + kPermThreads / 32) * sizeof(int32_t);
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        perm_scatter_kernel<<<nchunks, kPermThreads, smem, s>>>(topk_ids, n, topk, E, counts,
+                                                                gather_rows, dst_rows);
+        NVFP4_CHECK_LAUNCH();
+    }
+    return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,342 @@
+// quantize.cu -- per-token two-level NVFP4 quantization (rows), the per-tensor
+// variant, and the column-wise copy for the backward pass.
+//
+// Row kernel: one warp per row, 16-byte coalesced loads, the whole row held in
+// registers so the amax (found with bf16x2 max and warp shuffles) is reused for
+// the outer scale, the block scales and the encode without re-reading HBM
+// ("Towards Blackwell-Native 8-bit and 4-bit RL", "Online per-token scale": the
+// per-token FP32 scale is computed inside the quantize kernel and returned by the
+// same call; "miniTE report", "Transformer Engine path optimisation": amax reuse).
+// Lane l holds 8-element chunks l, l+32, ...; a 16-element block is the chunk
+// pair (2j, 2j+1) held by lanes 2j and 2j+1, so block maxima need one shuffle.
+#include "rowquant.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kRowThreads = 256;            // 8 warps = 8 rows per block iteration
+
+enum RowMode { kPerToken = 0, kPerTensor = 1, kAmaxOnly = 2 };
+
+struct RowParams {
+    const uint16_t* x;
+    int64_t rows_in;
+    int64_t ld_x;
+    const int32_t* gather;
+    int64_t rows_out;
+    int64_t rows_pad;   // rows_out rounded up to 128 (rows of the swizzled scales)
+    uint32_t* q;        // packed codes viewed as 32-bit words (8 codes each)
+    uint8_t* sf;
+    float* s;
+    unsigned* amax_ws;  // global amax as float bits (non-negative floats order as unsigned)
+    unsigned* status;
+    int cols;
+    int kgroups;        // 4-block groups per row = scale words per row
+};
+
+__device__ __forceinline__ int64_t source_row(const RowParams& p, int64_t r) {
+    int64_t src = p.gather ? static_cast<int64_t>(p.gather[r]) : r;
+    if (src >= p.rows_in) {
+        record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
+        src = -1;
+    }
+    return src;
+}
+
+// Row kernel with the row held in registers: NCH chunks of 8 per lane (cols <= 256 * NCH).
+template <int NCH, int MODE>
+__global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(RowParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kRowThreads / 32);
+    const int nchunks = p.cols >> 3;
+    const float tensor_amax = (MODE == kPerTensor) ? __uint_as_float(*p.amax_ws) : 0.0f;
+    const int64_t row_end = (MODE == kAmaxOnly) ? p.rows_out : p.rows_pad;
+    float seen_amax = 0.0f;
+
+    for (int64_t r = warp0; r < row_end; r += nwarps) {
+        if (r >= p.rows_out) {
+            zero_sf_row(p.sf, p.kgroups, r, lane);
+            continue;
+        }
+        const int64_t src = source_row(p, r);
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (src < 0 ? 0 : src) * p.ld_x);
+        uint4 v[NCH];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            const int c = i * 32 + lane;
+            v[i] = (src >= 0 && c < nchunks) ? ldg_stream(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float bmax[NCH];
+        const float row_amax = row_block_max<NCH>(v, bmax);
+        seen_amax = fmaxf(seen_amax, row_amax);
+        if (MODE == kAmaxOnly) continue;
+        encode_row<NCH>(v, bmax, MODE == kPerTensor ? tensor_amax : row_amax, nchunks, p.kgroups,
+                        p.q, p.sf, p.s, r, lane);
+    }
+    if (MODE != kPerTensor && p.amax_ws != nullptr && lane == 0 && seen_amax > 0.0f)
+        atomicMax(p.amax_ws, __float_as_uint(seen_amax));
+}
+
+// Rows longer than 256 * 16 elements: two passes over the row (the second from L1/L2).
+template <int MODE>
+__global__ void __launch_bounds__(kRowThreads) quant_rows_long_kernel(RowParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kRowThreads / 32);
+    const int nchunks = p.cols >> 3;
+    const int rounds = (nchunks + 31) / 32;
+    const float tensor_amax = (MODE == kPerTensor) ? __uint_as_float(*p.amax_ws) : 0.0f;
+    const int64_t row_end = (MODE == kAmaxOnly) ? p.rows_out : p.rows_pad;
+    float seen_amax = 0.0f;
+
+    for (int64_t r = warp0; r < row_end; r += nwarps) {
+        if (r >= p.rows_out) {
+            zero_sf_row(p.sf, p.kgroups, r, lane);
+            continue;
+        }
+        const int64_t src = source_row(p, r);
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (src < 0 ? 0 : src) * p.ld_x);
+        float row_amax = 0.0f;
+        for (int i = 0; i < rounds; ++i) {
+            const int c = i * 32 + lane;
+            if (src >= 0 && c < nchunks) row_amax = fmaxf(row_amax, chunk_absmax(__ldg(xr + c)));
+        }
+        row_amax = warp_max(row_amax);
+        seen_amax = fmaxf(seen_amax, row_amax);
+        if (MODE == kAmaxOnly) continue;
+        const ScaleRecipe rec(MODE == kPerTensor ? tensor_amax : row_amax);
+        uint32_t* qrow = p.q + r * nchunks;
+        for (int i = 0; i < rounds; ++i) {
+            const int c = i * 32 + lane;
+            const uint4 v = (src >= 0 && c < nchunks) ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+            const float m8 = chunk_absmax(v);
+            const float bm = fmaxf(m8, __shfl_xor_sync(0xFFFFFFFFu, m8, 1));
+            float rb;
+            const uint32_t sb = rec.block(bm, &rb);
+            const uint32_t w = encode_chunk(v, rb);
+            if (c < nchunks) qrow[c] = w;
+            store_sf_word(p.sf, p.kgroups, r, i, lane, sb);
+        }
+        if (lane == 0) p.s[r] = rec.S;
+    }
+    if (MODE != kPerTensor && p.amax_ws != nullptr && lane == 0 && seen_amax > 0.0f)
+        atomicMax(p.amax_ws, __float_as_uint(seen_amax));
+}
+
+// ---------------------------------------------------------------------------
+// Column-wise copy: X^T quantized along tokens with the per-tensor scale.
+// A warp owns 64 columns (2 per lane, read as bf16x2 so each token row is one
+// 128-byte load) and 64 tokens = 4 blocks of 16 = one scale word per column.
+// ---------------------------------------------------------------------------
+struct ColParams {
+    const uint16_t* x;
+    int64_t rows_in;
+    int64_t ld_x;
+    const int32_t* gather;
+    int64_t rows_out;   // tokens, % 16 == 0
+    uint8_t* q;         // [cols, rows_out / 2]
+    uint8_t* sf;        // swizzled [round_up(cols, 128), round_up(rows_out / 16, 4)]
+    float* s;
+    const unsigned* amax_ws;
+    unsigned* status;
+    int cols;
+    int kgroups;        // scale words per column row = ceil(rows_out / 64)
+};
+
+constexpr int kColThreads = 128;
+
+__global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int k0 = blockIdx.x * 64 + lane * 2;
+    const int g = blockIdx.y * (kColThreads / 32) + warp;   // token group of 64
+    if (g >= p.kgroups) return;
+    const int64_t m0 = static_cast<int64_t>(g) * 64;
+    const bool col_ok = k0 < p.cols;
+    const ScaleRecipe rec(__uint_as_float(*p.amax_ws));
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.s[0] = rec.S;
+
+    uint32_t v[64];
+#pragma unroll
+    for (int t = 0; t < 64; ++t) {
+        const int64_t m = m0 + t;
+        int64_t src = -1;
+        if (m < p.rows_out) {
+            src = p.gather ? static_cast<int64_t>(p.gather[m]) : m;
+            if (src >= p.rows_in) src = -1;   // reported by the row pass
+        }
+        v[t] = (col_ok && src >= 0)
+                   ? __ldg(reinterpret_cast<const uint32_t*>(p.x + src * p.ld_x + k0))
+                   : 0u;
+    }
+    uint32_t word0 = 0u, word1 = 0u;
+    const int64_t qstride = p.rows_out >> 1;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            a0 = fmaxf(a0, fabsf(bf16lo(v[16 * b + t])));
+            a1 = fmaxf(a1, fabsf(bf16hi(v[16 * b + t])));
+        }
+        float r0, r1;
+        const uint32_t s0 = rec.block(a0, &r0);
+        const uint32_t s1 = rec.block(a1, &r1);
+        word0 |= s0 << (8 * b);
+        word1 |= s1 << (8 * b);
+        const uint32_t* vb = v + 16 * b;
+        uint2 c0, c1;
+        c0.x = cvt_e2m1x8(__fmul_rn(bf16lo(vb[0]), r0), __fmul_rn(bf16lo(vb[1]), r0),
+                          __fmul_rn(bf16lo(vb[2]), r0), __fmul_rn(bf16lo(vb[3]), r0),
+                          __fmul_rn(bf16lo(vb[4]), r0), __fmul_rn(bf16lo(vb[5]), r0),
+                          __fmul_rn(bf16lo(vb[6]), r0), __fmul_rn(bf16lo(vb[7]), r0));
+        c0.y = cvt_e2m1x8(__fmul_rn(bf16lo(vb[8]), r0), __fmul_rn(bf16lo(vb[9]), r0),
+                          __fmul_rn(bf16lo(vb[10]), r0), __fmul_rn(bf16lo(vb[11]), r0),
+                          __fmul_rn(bf16lo(vb[12]), r0), __fmul_rn(bf16lo(vb[13]), r0),
+                          __fmul_rn(bf16lo(vb[14]), r0), __fmul_rn(bf16lo(vb[15]), r0));
+        c1.x = cvt_e2m1x8(__fmul_rn(bf16hi(vb[0]), r1), __fmul_rn(bf16hi(vb[1]), r1),
+                          __fmul_rn(bf16hi(vb[2]), r1), __fmul_rn(bf16hi(vb[3]), r1),
+                          __fmul_rn(bf16hi(vb[4]), r1), __fmul_rn(bf16hi(vb[5]), r1),
+                          __fmul_rn(bf16hi(vb[6]), r1), __fmul_rn(bf16hi(vb[7]), r1));
+        c1.y = cvt_e2m1x8(__fmul_rn(bf16hi(vb[8]), r1), __fmul_rn(bf16hi(vb[9]), r1),
+                          __fmul_rn(bf16hi(vb[10]), r1), __fmul_rn(bf16hi(vb[11]), r1),
+                          __fmul_rn(bf16hi(vb[12]), r1), __fmul_rn(bf16hi(vb[13]), r1),
+                          __fmul_rn(bf16hi(vb[14]), r1), __fmul_rn(bf16hi(vb[15]), r1));
+        const int64_t mb = m0 + 16 * b;
+        if (col_ok && mb < p.rows_out) {
+            *reinterpret_cast<uint2*>(p.q + k0 * qstride + (mb >> 1)) = c0;
+            *reinterpret_cast<uint2*>(p.q + (k0 + 1) * qstride + (mb >> 1)) = c1;
+        }
+    }
+    // scale words (padding columns k >= cols get zero words)
+    *reinterpret_cast<uint32_t*>(p.sf + sf_word_offset(k0, g, p.kgroups)) = col_ok ? word0 : 0u;
+    *reinterpret_cast<uint32_t*>(p.sf + sf_word_offset(k0 + 1, g, p.kgroups)) = col_ok ? word1 : 0u;
+}
+
+template <int MODE>
+nvfp4_status launch_rows(const RowParams& p, int blocks, cudaStream_t s) {
+    const int need = (p.cols / 8 + 31) / 32;
+    if (need <= 1) quant_rows_kernel<1, MODE><<<blocks, kRowThreads, 0, s>>>(p);
+    else if (need <= 2) quant_rows_kernel<2, MODE><<<blocks, kRowThreads, 0, s>>>(p);
+    else if (need <= 4) quant_rows_kernel<4, MODE><<<blocks, kRowThreads, 0, s>>>(p);
+    else if (need <= 8) quant_rows_kernel<8, MODE><<<blocks, kRowThreads, 0, s>>>(p);
+    else if (need <= 12) quant_rows_kernel<12, MODE><<<blocks, kRowThreads, 0, s>>>(p);
+    else if (need <= 16) quant_rows_kernel<16, MODE><<<blocks, kRowThreads, 0, s>>>(p);
+    else quant_rows_long_kernel<MODE><<<blocks, kRowThreads, 0, s>>>(p);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+// Shared by the ABI entry and by the SwiGLU file's requantize check.
+nvfp4_status quantize_rows_launch(const uint16_t* x, int64_t rows_in, int64_t cols, int64_t ld_x,
+                                  const int32_t* gather, int64_t rows_out, int mode, void* q,
+                                  void* sf, float* s, unsigned* amax_ws, bool publish_amax,
+                                  const DeviceCtx& ctx, cudaStream_t stream) {
+    RowParams p;
+    p.x = x;
+    p.rows_in = rows_in;
+    p.ld_x = ld_x;
+    p.gather = gather;
+    p.rows_out = rows_out;
+    p.rows_pad = round_up(rows_out, 128);
+    p.q = static_cast<uint32_t*>(q);
+    p.sf = static_cast<uint8_t*>(sf);
+    p.s = s;
+    p.amax_ws = (mode == kPerTensor || publish_amax) ? amax_ws : nullptr;
+    p.status = ctx.status;
+    p.cols = static_cast<int>(cols);
+    p.kgroups = static_cast<int>(round_up(cols / 16, 4) / 4);
+    const int64_t rows_launch = (mode == kAmaxOnly) ? rows_out : p.rows_pad;
+    if (rows_launch == 0) return NVFP4_OK;
+    const int64_t want = ceil_div(rows_launch, kRowThreads / 32);
+    const int blocks = static_cast<int>(want < 1048576 ? want : 1048576);
+    if (mode == kPerToken) return launch_rows<kPerToken>(p, blocks, stream);
+    if (mode == kPerTensor) return launch_rows<kPerTensor>(p, blocks, stream);
+    return launch_rows<kAmaxOnly>(p, blocks, stream);
+}
+
+nvfp4_status quantize_cols_launch(const uint16_t* x, int64_t rows_in, int64_t cols, int64_t ld_x,
+                                  const int32_t* gather, int64_t rows_out, void* q, void* sf,
+                                  float* s, const unsigned* amax_ws, const DeviceCtx& ctx,
+                                  cudaStream_t stream) {
+    ColParams p;
+    p.x = x;
+    p.rows_in = rows_in;
+    p.ld_x = ld_x;
+    p.gather = gather;
+    p.rows_out = rows_out;
+    p.q = static_cast<uint8_t*>(q);
+    p.sf = static_cast<uint8_t*>(sf);
+    p.s = s;
+    p.amax_ws = amax_ws;
+    p.status = ctx.status;
+    p.cols = static_cast<int>(cols);
+    p.kgroups = static_cast<int>(ceil_div(rows_out, 64));
+    if (p.kgroups == 0) {
+        return cudaMemsetAsync(s, 0, sizeof(float), stream) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+    }
+    dim3 grid(static_cast<unsigned>(round_up(cols, 128) / 64),
+              static_cast<unsigned>(ceil_div(p.kgroups, kColThreads / 32)));
+    quant_cols_kernel<<<grid, kColThreads, 0, stream>>>(p);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+size_t nvfp4_quantize_workspace_bytes(void) { return 256; }
+
+nvfp4_status nvfp4_quantize_per_token(const void* x, int64_t rows_in, int64_t cols, int64_t ld_x,
+                                      const int32_t* gather_rows, int64_t rows_out,
+                                      nvfp4_scale_mode mode, void* q_row, void* sf_row,
+                                      float* s_row, void* q_col, void* sf_col, float* s_col,
+                                      void* workspace, size_t workspace_bytes,
+                                      nvfp4_stream_t stream) {
+    DeviceCtx ctx;
+    nvfp4_status st = device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
+    if (mode != NVFP4_SCALE_PER_TOKEN && mode != NVFP4_SCALE_PER_TENSOR) return NVFP4_ERR_INVALID_ARG;
+    if (rows_in < 0 || rows_out < 0 || cols <= 0) return NVFP4_ERR_SHAPE;
+    if (cols % 16 != 0 || cols > (int64_t(1) << 24) || ld_x < cols || ld_x % 8 != 0) return NVFP4_ERR_SHAPE;
+    if (gather_rows == nullptr && rows_out > rows_in) return NVFP4_ERR_SHAPE;
+    const bool want_col = (q_col != nullptr) || (sf_col != nullptr) || (s_col != nullptr);
+    if (want_col && (q_col == nullptr || sf_col == nullptr || s_col == nullptr)) return NVFP4_ERR_INVALID_ARG;
+    if (want_col && rows_out % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (rows_out > 0 && (q_row == nullptr || sf_row == nullptr || s_row == nullptr)) return NVFP4_ERR_INVALID_ARG;
+    if (rows_out > 0 && rows_in > 0 && x == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(sf_row, 16) || !aligned(s_row, 4) ||
+        !aligned(gather_rows, 4) || !aligned(q_col, 16) || !aligned(sf_col, 16) || !aligned(s_col, 4))
+        return NVFP4_ERR_ALIGNMENT;
+    const bool need_ws = want_col || mode == NVFP4_SCALE_PER_TENSOR;
+    if (need_ws && (workspace == nullptr || workspace_bytes < nvfp4_quantize_workspace_bytes()))
+        return NVFP4_ERR_WORKSPACE;
+    if (need_ws && !aligned(workspace, 4)) return NVFP4_ERR_ALIGNMENT;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    unsigned* amax_ws = static_cast<unsigned*>(workspace);
+    if (need_ws && cudaMemsetAsync(amax_ws, 0, sizeof(unsigned), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+
+    if (mode == NVFP4_SCALE_PER_TENSOR) {
+        st = quantize_rows_launch(xb, rows_in, cols, ld_x, gather_rows, rows_out, kAmaxOnly, nullptr,
+                                  nullptr, nullptr, amax_ws, true, ctx, s);
+        if (st != NVFP4_OK) return st;
+    }
+    st = quantize_rows_launch(xb, rows_in, cols, ld_x, gather_rows, rows_out, mode, q_row, sf_row,
+                              s_row, amax_ws, want_col && mode == NVFP4_SCALE_PER_TOKEN, ctx, s);
+    if (st != NVFP4_OK) return st;
+    if (want_col)
+        st = quantize_cols_launch(xb, rows_in, cols, ld_x, gather_rows, rows_out, q_col, sf_col,
+                                  s_col, amax_ws, ctx, s);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,286 @@
+"""Thin Python binding of libnvfp4 (include/nvfp4.h): argument marshalling only.
+
+Every function named nvfp4_* calls the C entry point of the same name with raw
+device pointers taken from torch tensors and the current CUDA stream; every
+step of the computation runs in the library's CUDA kernels.  The lower-case
+helpers (quantize, gemm, ...) only allocate the output tensors with torch and
+call those entry points.  If the library is not built the import of a helper
+fails loudly: there is no CPU or PyTorch fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+_LIB = None
+
+STATUS_NAMES = {
+    0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_ALIGNMENT", 3: "NVFP4_ERR_SHAPE",
+    4: "NVFP4_ERR_UNSUPPORTED_DEVICE", 5: "NVFP4_ERR_CUDA", 6: "NVFP4_ERR_TIMEOUT",
+    7: "NVFP4_ERR_DEVICE_INPUT", 8: "NVFP4_ERR_WORKSPACE",
+}
+PER_TOKEN, PER_TENSOR = 0, 1
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, where, status):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def library_path():
+    return _build.LIB
+
+
+def lib():
+    """Load libnvfp4.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libnvfp4.so is not built (expected {path}); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(path)
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    st = ctypes.c_int
+    sig = {
+        "nvfp4_packed_bytes": (SZ, [I64, I64]),
+        "nvfp4_sf_bytes": (SZ, [I64, I64]),
+        "nvfp4_quantize_workspace_bytes": (SZ, []),
+        "nvfp4_quantize_per_token": (st, [P, I64, I64, I64, P, I64, ctypes.c_int, P, P, P, P, P, P,
+                                          P, SZ, P]),
+        "nvfp4_moe_capacity": (I64, [I64, I32, I32, I32]),
+        "nvfp4_moe_permute_workspace_bytes": (SZ, [I64, I32, I32]),
+        "nvfp4_moe_permute": (st, [P, I64, I32, I32, I32, P, P, I64, P, P, SZ, P]),
+        "nvfp4_gemm": (st, [P, P, P, I64, P, P, P, I64, I64, P, I64, P]),
+        "nvfp4_grouped_gemm": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
+        "nvfp4_swiglu_quantize": (st, [P, I64, I64, I64, P, P, P, P, P, P]),
+        "nvfp4_get_device_status": (st, [P]),
+        "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "nvfp4_debug_cvt_probe": (st, [P, P, P, P]),
+        "nvfp4_debug_wait_timeout": (st, [I64, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = L
+    return L
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _s(stream):
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+
+def _ok(name, status):
+    if status != 0:
+        raise NVFP4Error(name, status)
+
+
+# ---------------------------------------------------------------------------
+# The C entry points, one to one
+# ---------------------------------------------------------------------------
+
+def nvfp4_packed_bytes(rows, cols):
+    return lib().nvfp4_packed_bytes(rows, cols)
+
+
+def nvfp4_sf_bytes(rows, cols):
+    return lib().nvfp4_sf_bytes(rows, cols)
+
+
+def nvfp4_quantize_workspace_bytes():
+    return lib().nvfp4_quantize_workspace_bytes()
+
+
+def nvfp4_quantize_per_token(x, rows_in, cols, ld_x, gather_rows, rows_out, mode, q_row, sf_row,
+                             s_row, q_col=None, sf_col=None, s_col=None, workspace=None,
+                             workspace_bytes=0, stream=None):
+    _ok("nvfp4_quantize_per_token", lib().nvfp4_quantize_per_token(
+        _p(x), rows_in, cols, ld_x, _p(gather_rows), rows_out, mode, _p(q_row), _p(sf_row),
+        _p(s_row), _p(q_col), _p(sf_col), _p(s_col), _p(workspace), workspace_bytes, _s(stream)))
+
+
+def nvfp4_moe_capacity(tokens, topk, num_experts, row_align):
+    return lib().nvfp4_moe_capacity(tokens, topk, num_experts, row_align)
+
+
+def nvfp4_moe_permute_workspace_bytes(tokens, topk, num_experts):
+    return lib().nvfp4_moe_permute_workspace_bytes(tokens, topk, num_experts)
+
+
+def nvfp4_moe_permute(topk_ids, tokens, topk, num_experts, row_align, expert_offsets, gather_rows,
+                      capacity, dst_rows, workspace, workspace_bytes, stream=None):
+    _ok("nvfp4_moe_permute", lib().nvfp4_moe_permute(
+        _p(topk_ids), tokens, topk, num_experts, row_align, _p(expert_offsets), _p(gather_rows),
+        capacity, _p(dst_rows), _p(workspace), workspace_bytes, _s(stream)))
+
+
+def nvfp4_gemm(a_q, a_sf, a_s, M, b_q, b_sf, b_s, N, K, y, ld_y, stream=None):
+    _ok("nvfp4_gemm", lib().nvfp4_gemm(_p(a_q), _p(a_sf), _p(a_s), M, _p(b_q), _p(b_sf), _p(b_s),
+                                       N, K, _p(y), ld_y, _s(stream)))
+
+
+def nvfp4_grouped_gemm(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_sf, b_s, N, K, y,
+                       stream=None):
+    _ok("nvfp4_grouped_gemm", lib().nvfp4_grouped_gemm(
+        _p(a_q), _p(a_sf), _p(a_s), rows_capacity, _p(expert_offsets), E, _p(b_q), _p(b_sf),
+        _p(b_s), N, K, _p(y), _s(stream)))
+
+
+def nvfp4_swiglu_quantize(y1, rows, ffn, ld_y1, row_count, q, sf, s, h=None, stream=None):
+    _ok("nvfp4_swiglu_quantize", lib().nvfp4_swiglu_quantize(
+        _p(y1), rows, ffn, ld_y1, _p(row_count), _p(q), _p(sf), _p(s), _p(h), _s(stream)))
+
+
+def nvfp4_get_device_status(stream=None):
+    return lib().nvfp4_get_device_status(_s(stream))
+
+
+def nvfp4_status_string(status):
+    return lib().nvfp4_status_string(status).decode()
+
+
+def nvfp4_debug_cvt_probe(first, last, counters, stream=None):
+    _ok("nvfp4_debug_cvt_probe", lib().nvfp4_debug_cvt_probe(_p(first), _p(last), _p(counters),
+                                                            _s(stream)))
+
+
+def nvfp4_debug_wait_timeout(timeout_ns, stream=None):
+    _ok("nvfp4_debug_wait_timeout", lib().nvfp4_debug_wait_timeout(timeout_ns, _s(stream)))
+
+
+# ---------------------------------------------------------------------------
+# Helpers that allocate outputs with torch and call the entry points above
+# ---------------------------------------------------------------------------
+
+def _u8(n, dev):
+    return torch.empty(n, dtype=torch.uint8, device=dev)
+
+
+class Workspace:
+    """Caller-owned scratch buffer reused across calls on one stream."""
+
+    def __init__(self, device, nbytes=0):
+        self.device = device
+        self.buf = _u8(max(int(nbytes), 256), device)
+
+    def get(self, nbytes):
+        if self.buf.numel() < nbytes:
+            self.buf = _u8(int(nbytes), self.device)
+        return self.buf
+
+
+def quantize(x, gather=None, rows_out=None, mode="per_token", column_copy=False, workspace=None,
+             stream=None):
+    """Quantize the rows of a bf16 [rows, K] CUDA tensor; returns a dict of
+    device tensors q [rows_out, K/2] uint8, sf (swizzled bytes), s [rows_out]
+    float32, and with column_copy q_col / sf_col / s_col."""
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2
+    rows_in, K = x.shape
+    ld = x.stride(0)
+    assert x.stride(1) == 1
+    if gather is not None:
+        rows_out = gather.numel() if rows_out is None else rows_out
+    elif rows_out is None:
+        rows_out = rows_in
+    dev = x.device
+    out = dict(rows=rows_out, cols=K,
+               q=_u8((rows_out, K // 2), dev), sf=_u8(nvfp4_sf_bytes(rows_out, K), dev),
+               s=torch.empty(rows_out, dtype=torch.float32, device=dev))
+    qc = sfc = sc = None
+    if column_copy:
+        qc = _u8((K, rows_out // 2), dev)
+        sfc = _u8(nvfp4_sf_bytes(K, rows_out), dev)
+        sc = torch.empty(1, dtype=torch.float32, device=dev)
+        out.update(q_col=qc, sf_col=sfc, s_col=sc)
+    m = PER_TENSOR if mode == "per_tensor" else PER_TOKEN
+    ws = None
+    wsb = 0
+    if column_copy or m == PER_TENSOR:
+        wsb = nvfp4_quantize_workspace_bytes()
+        ws = (workspace or Workspace(dev)).get(wsb)
+    nvfp4_quantize_per_token(x, rows_in, K, ld, gather, rows_out, m, out["q"], out["sf"], out["s"],
+                             qc, sfc, sc, ws, wsb, stream)
+    return out
+
+
+def gemm(a, b, out=None, stream=None):
+    """Y = a @ b^T (bf16) from two quantize() results (a: [M, K], b: [N, K])."""
+    M, K = a["rows"], a["cols"]
+    N = b["rows"]
+    assert b["cols"] == K
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a["q"].device)
+    nvfp4_gemm(a["q"], a["sf"], a["s"], M, b["q"], b["sf"], b["s"], N, K, y, y.stride(0), stream)
+    return y
+
+
+def moe_permute(topk_ids, num_experts, row_align=128, workspace=None, stream=None):
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    cap = nvfp4_moe_capacity(T, k, num_experts, row_align)
+    off = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    gather = torch.empty(cap, dtype=torch.int32, device=dev)
+    dst = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wsb = nvfp4_moe_permute_workspace_bytes(T, k, num_experts)
+    ws = (workspace or Workspace(dev)).get(wsb)
+    nvfp4_moe_permute(topk_ids, T, k, num_experts, row_align, off, gather, cap, dst, ws, wsb, stream)
+    return dict(offsets=off, gather=gather, dst=dst, capacity=cap)
+
+
+def quantize_experts(w, stream=None):
+    """Quantize stacked expert weights w [E, N, K] (bf16) per output row into the
+    grouped GEMM's weight format: q [E, N, K/2], sf (E blocks of
+    nvfp4_sf_bytes(N, K) bytes), s [E, N]."""
+    E, N, K = w.shape
+    dev = w.device
+    sfb = nvfp4_sf_bytes(N, K)
+    q = _u8((E, N, K // 2), dev)
+    sf = _u8(E * sfb, dev)
+    s = torch.empty((E, N), dtype=torch.float32, device=dev)
+    flat = w.reshape(E * N, K)
+    if N % 128 == 0:
+        # 128-row scale tiles never straddle experts: one call lays out every block
+        nvfp4_quantize_per_token(flat, E * N, K, K, None, E * N, PER_TOKEN, q, sf, s, stream=stream)
+    else:
+        for e in range(E):
+            nvfp4_quantize_per_token(flat[e * N:(e + 1) * N], N, K, K, None, N, PER_TOKEN, q[e],
+                                     sf.data_ptr() + e * sfb, s[e], stream=stream)
+    return dict(rows=N, cols=K, experts=E, q=q, sf=sf, s=s)
+
+
+def grouped_gemm(a, expert_offsets, num_experts, b_q, b_sf, b_s, N, K, out=None, stream=None):
+    rows = a["rows"]
+    y = out if out is not None else torch.empty((rows, N), dtype=torch.bfloat16, device=a["q"].device)
+    nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], rows, expert_offsets, num_experts, b_q, b_sf, b_s,
+                       N, K, y, stream)
+    return y
+
+
+def swiglu_quantize(y1, ffn, row_count=None, want_h=False, stream=None):
+    rows = y1.shape[0]
+    dev = y1.device
+    out = dict(rows=rows, cols=ffn, q=_u8((rows, ffn // 2), dev),
+               sf=_u8(nvfp4_sf_bytes(rows, ffn), dev),
+               s=torch.empty(rows, dtype=torch.float32, device=dev))
+    h = torch.empty((rows, ffn), dtype=torch.bfloat16, device=dev) if want_h else None
+    nvfp4_swiglu_quantize(y1, rows, ffn, y1.stride(0), row_count, out["q"], out["sf"], out["s"], h,
+                          stream)
+    if want_h:
+        out["h"] = h
+    return out
+
+
+def get_device_status(stream=None):
+    return nvfp4_get_device_status(stream)

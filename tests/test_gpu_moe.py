@@ -1,0 +1,132 @@
+"""GPU parity of the MoE path: routing permute (bit-exact), gather-quantize into
+the padded per-expert layout (bit-exact), fused SwiGLU + quantize, and the
+grouped W4A4 GEMM (tolerance of the dense GEMM), each on seeded inputs that
+the oracle also receives.  Workload: Qwen3-30B-A3B-shaped experts (hidden 2048,
+expert FFN 768, 128 experts, top-8), as on "Towards Blackwell-Native 8-bit and
+4-bit RL" ("Experimental setup": Qwen3-30B-A3B; routed experts fc1 / fc2 are
+the NVFP4 layers of the recipe).
+"""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_precision_rl_gb300 import workloads as W
+from _gpu_util import assert_quant_equal, bf16_to_f64, bf16_ulp, check_gemm, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _ids(seed, T, E, k):
+    return W.route_topk(np.random.default_rng(seed), T, E, k)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 4, 1), (37, 8, 2), (300, 16, 4), (40, 64, 2),
+                                   (4096, 128, 8), (65536, 128, 8)])
+def test_permute_bit_exact(nv, orc, T, E, k):
+    ids = _ids(T + E, T, E, k)
+    got = nv.moe_permute(torch.from_numpy(ids).cuda(), E)
+    ref = orc.moe_permute(ids, E, 128, capacity=got["capacity"])
+    assert np.array_equal(host(got["offsets"]), ref["offsets"])
+    assert np.array_equal(host(got["gather"]), ref["gather"])
+    assert np.array_equal(host(got["dst"]), ref["dst"])
+    assert nv.nvfp4_get_device_status() == 0
+
+
+def test_permute_reports_bad_ids(nv):
+    ids = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32, device="cuda")
+    got = nv.moe_permute(ids, 4)
+    assert nv.nvfp4_get_device_status() == 7          # NVFP4_ERR_DEVICE_INPUT
+    dst = host(got["dst"])
+    assert dst[1, 1] == -1 and (dst[0] >= 0).all()
+
+
+def test_gather_quantize_bit_exact(nv, orc):
+    T, H, E, k = 300, 512, 16, 4
+    x = W.small_matrix(21, T, H)
+    ids = _ids(22, T, E, k)
+    perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E)
+    rperm = orc.moe_permute(ids, E, 128, capacity=perm["capacity"])
+    got = nv.quantize(to_dev(x), gather=perm["gather"])
+    ref = orc.quantize(x, gather=rperm["gather"])
+    assert_quant_equal(got, ref, what="gather-quantize")
+
+
+@pytest.mark.parametrize("R,F", [(300, 768), (129, 64), (64, 2048)])
+def test_swiglu_quantize(nv, orc, R, F):
+    rng = np.random.default_rng(R + F)
+    y1 = W.to_bf16_bits((rng.standard_normal((R, 2 * F)) * 2).astype(np.float32))
+    got = nv.swiglu_quantize(to_dev(y1), F, want_h=True)
+    h_ref = orc.swiglu(y1, F)
+    hg = bf16_to_f64(got["h"])
+    hr = W.bf16_bits_to_float(h_ref).astype(np.float64)
+    assert np.all(np.abs(hg - hr) <= bf16_ulp(hr)), "h differs by more than one bf16 ulp"
+    # rows whose h agrees exactly quantize bit-exactly; the fused quantize is
+    # the row quantizer's own code, checked against the GPU row quantizer too
+    ref = orc.quantize(h_ref)
+    same = np.all(host(got["h"]).view(np.uint16) == h_ref, axis=1)
+    assert same.mean() > 0.5
+    assert_quant_equal(got, ref, rows=np.nonzero(same)[0], what="swiglu rows")
+    again = nv.quantize(got["h"])
+    assert torch.equal(again["q"], got["q"]) and torch.equal(again["sf"], got["sf"])
+    assert torch.equal(again["s"], got["s"])
+
+
+def test_swiglu_row_count(nv):
+    R, F = 256, 256
+    y1 = torch.randn(R, 2 * F, device="cuda").to(torch.bfloat16)
+    rc = torch.tensor([200], dtype=torch.int32, device="cuda")
+    got = nv.swiglu_quantize(y1, F, row_count=rc, want_h=True)
+    assert not got["h"][200:].any() and not got["q"][200:].any() and not got["s"][200:].any()
+    assert got["s"][:200].gt(0).all()
+
+
+def _grouped_case(nv, orc, T, H, N, E, k, seed, sample=None, experts_checked=None):
+    x = W.small_matrix(seed, T, H)
+    w = W.small_matrix(seed + 1, E * N, H, std=0.02).reshape(E, N, H)
+    ids = _ids(seed + 2, T, E, k)
+    perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E)
+    a = nv.quantize(to_dev(x), gather=perm["gather"])
+    wq = nv.quantize_experts(to_dev(w.reshape(E * N, H)).reshape(E, N, H))
+    y = nv.grouped_gemm(a, perm["offsets"], E, wq["q"], wq["sf"], wq["s"], N, H)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_status() == 0
+    rperm = orc.moe_permute(ids, E, 128, capacity=perm["capacity"])
+    off = rperm["offsets"]
+    ra = orc.quantize(x, gather=rperm["gather"])
+    yg = bf16_to_f64(y)
+    experts = range(E) if experts_checked is None else experts_checked
+    for e in experts:
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        rw = orc.quantize(w[e])
+        ae = orc.rows_of(ra, r0, r1)
+        if sample is None:
+            yref, absy = orc.gemm_exact(ae, rw, with_abs=True)
+            check_gemm(yg[r0:r1], yref, absy, H, f"expert {e}")
+        else:
+            rng = np.random.default_rng(e)
+            mi = rng.integers(0, r1 - r0, sample)
+            ni = rng.integers(0, N, sample)
+            yref, absy = orc.gemm_exact_sampled(ae, rw, mi, ni)
+            check_gemm(yg[r0 + mi, ni], yref, absy, H, f"expert {e}")
+        pad = rperm["gather"][r0:r1] < 0
+        assert not yg[r0:r1][pad].any()
+
+
+@pytest.mark.parametrize("T,H,N,E,k", [(300, 256, 384, 16, 4), (40, 512, 256, 64, 2),
+                                       (500, 768, 272, 8, 2)])
+def test_grouped_gemm_small(nv, orc, T, H, N, E, k):
+    _grouped_case(nv, orc, T, H, N, E, k, seed=T + N)
+
+
+def test_grouped_fc1_config3_sampled(nv, orc):
+    """fc1 (gate+up, K=2048 -> N=1536) at the full 4096-token, 128-expert size."""
+    _grouped_case(nv, orc, 4096, 2048, 1536, 128, 8, seed=31, sample=400,
+                  experts_checked=[0, 1, 37, 64, 100, 127])
+
+
+def test_grouped_fc2_config3_sampled(nv, orc):
+    """fc2 (down, K=768 -> N=2048) at the full size, on seeded expert inputs."""
+    _grouped_case(nv, orc, 4096, 768, 2048, 128, 8, seed=41, sample=400,
+                  experts_checked=[0, 5, 63, 127])
