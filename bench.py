@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Benchmark of the per-token NVFP4 W4A4 linear-layer hot path on GB300.
+
+One step = one pass of the dense learner path on the Qwen3-4B MLP
+up-projection workload (X [4096, 2560] bf16, seq 4096 x micro-batch 1,
+W [9728, 2560]):
+    per-token quantize of X (row-wise + column-wise copy for the backward),
+    per-row quantize of W, block-scaled W4A4 GEMM -> Y bf16 [4096, 9728].
+The same run also times the MoE expert step (Qwen3-30B-A3B shapes, 4096
+tokens, 128 experts, top-8): routing permute, gather-quantize, grouped fc1,
+fused SwiGLU + quantize, grouped fc2 (reported under "moe").
+
+value  = GEMM algorithmic FLOP (2 M N K, all ranks) / device step time
+         (CUDA events on the launching stream; L2 flushed before every step).
+e2e    = the same metric through the library calls with HOST buffers: pinned
+         X copied in, Y copied out, inside the timed region.
+roofline = the dominant kernel (the GEMM): achieved FLOP/s against the FP4 peak
+         derived from the measured bf16 peak (x6, the 13.5/2.25 nominal ratio).
+
+--impl reference times the CPU oracle (oracle/) on a bounded sample of the
+same workload on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, N, K = 4096, 9728, 2560
+WORKLOAD = "qwen3_4b_up_proj_4096x9728x2560"
+METRIC = "W4A4 GEMM TFLOPS (% of 9 PF FP4) and per-token quantize GB/s (% of HBM)"
+PAGES_FP4_PF = 9.0          # the target denominator named with the metric
+NOMINAL_FP4_PF = 13.5       # the pages' B300 dense FP4 row
+BF16_TO_FP4 = 13.5 / 2.25   # nominal dense FP4 / BF16 ratio
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-moe", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def gemm_traffic(kernel_sha):
+    """dram bytes per GEMM launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("gemm_cu_sha256") != kernel_sha or d.get("workload") != WORKLOAD:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [ln.strip().split(",") for ln in self.tmp.read().splitlines() if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from nvfp4_precision_rl_gb300 import _build
+    from nvfp4_precision_rl_gb300 import ops
+    from nvfp4_precision_rl_gb300 import workloads as W
+
+    _build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    wl = W.config2()
+    x = to_dev(wl.x)
+    w = to_dev(wl.w)
+    ws = ops.Workspace(dev)
+    # outputs, allocated once
+    qx = dict(rows=M, cols=K, q=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+              sf=torch.empty(ops.nvfp4_sf_bytes(M, K), dtype=torch.uint8, device=dev),
+              s=torch.empty(M, dtype=torch.float32, device=dev))
+    qcol = torch.empty((K, M // 2), dtype=torch.uint8, device=dev)
+    sfcol = torch.empty(ops.nvfp4_sf_bytes(K, M), dtype=torch.uint8, device=dev)
+    scol = torch.empty(1, dtype=torch.float32, device=dev)
+    qw = dict(rows=N, cols=K, q=torch.empty((N, K // 2), dtype=torch.uint8, device=dev),
+              sf=torch.empty(ops.nvfp4_sf_bytes(N, K), dtype=torch.uint8, device=dev),
+              s=torch.empty(N, dtype=torch.float32, device=dev))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    wsb = ops.nvfp4_quantize_workspace_bytes()
+    wsbuf = ws.get(wsb)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def quant_x(src):
+        ops.nvfp4_quantize_per_token(src, M, K, K, None, M, ops.PER_TOKEN, qx["q"], qx["sf"], qx["s"],
+                                     qcol, sfcol, scol, wsbuf, wsb, stream)
+
+    def quant_w():
+        ops.nvfp4_quantize_per_token(w, N, K, K, None, N, ops.PER_TOKEN, qw["q"], qw["sf"], qw["s"],
+                                     stream=stream)
+
+    def gemm():
+        ops.nvfp4_gemm(qx["q"], qx["sf"], qx["s"], M, qw["q"], qw["sf"], qw["s"], N, K, y, N, stream)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        quant_x(x)
+        if evs:
+            evs[1].record(stream)
+        quant_w()
+        if evs:
+            evs[2].record(stream)
+        gemm()
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = ops.nvfp4_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {ops.STATUS_NAMES.get(st)}")
+
+    clocks = Clocks(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    steps_ev = []
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()                      # L2 flush, outside the timed events
+        evs = [ev() for _ in range(4)]
+        step(evs)
+        steps_ev.append(evs)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    t_step = np.array([e[0].elapsed_time(e[3]) for e in steps_ev])        # ms
+    t_qx = np.array([e[0].elapsed_time(e[1]) for e in steps_ev])
+    t_qw = np.array([e[1].elapsed_time(e[2]) for e in steps_ev])
+    t_gemm = np.array([e[2].elapsed_time(e[3]) for e in steps_ev])
+    ms_step = float(t_step.mean())
+    ms_step_max = ms_step
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_step_max = float(tt.item())
+    flop = 2.0 * M * N * K
+    value = world * flop / (ms_step_max * 1e-3) / 1e12
+
+    # ---- end to end through the library calls with host buffers ----
+    x_host = torch.from_numpy(wl.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    x_stage = torch.empty_like(x)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        x_stage.copy_(x_host, non_blocking=True)
+        quant_x(x_stage)
+        quant_w()
+        gemm()
+        y_host.copy_(y, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_step = float(np.mean(e2e_ms))
+    if world > 1:
+        tt = torch.tensor([e2e_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_step = float(tt.item())
+    e2e_value = world * flop / (e2e_step * 1e-3) / 1e12
+
+    hbm_gbs, bf16_burst, bf16_sust, peak_src = measured_peaks()
+    fp4_peak = bf16_burst * BF16_TO_FP4
+    gemm_tflops = flop / (t_gemm.mean() * 1e-3) / 1e12
+    # per-token quantize of X: algorithmic bytes = read 2 B/elem + write 0.5 B codes
+    # + 1/16 B scales per elem + 4 B per row; the column copy writes the same again
+    qx_bytes_row = M * K * 2 + M * K * 0.5 + M * K / 16 + M * 4
+    qx_bytes = qx_bytes_row + M * K * 0.5 + M * K / 16 + 4
+    qw_bytes = N * K * 2 + N * K * 0.5 + N * K / 16 + N * 4
+    qx_gbs = qx_bytes / (t_qx.mean() * 1e-3) / 1e9
+    qw_gbs = qw_bytes / (t_qw.mean() * 1e-3) / 1e9
+    sha = file_sha(os.path.join(ROOT, "nvfp4_precision_rl_gb300", "csrc", "gemm.cu"))
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3) -> fp32 acc -> bf16",
+        "data": "synthetic (seeded numpy PCG64, Qwen3-4B-shaped activations and weights)",
+        "config": {"workload": WORKLOAD, "M_tokens": M, "N": N, "K": K, "seq_len": 4096,
+                   "micro_batch": 1, "column_copy": True, "scale_mode": "per_token",
+                   "parallelism": f"dp{world} (independent batches, no collective)",
+                   "l2": "flushed (512 MB write) before every timed step"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(M * K * 2), "d2h_bytes_per_step": int(M * N * 2),
+                "ms_per_step": round(e2e_step, 5)},
+        "roofline": {"kernel": "nvfp4_gemm_kernel", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp4_peak, 4),
+                     "peak_basis": f"{peak_src} bf16 burst {bf16_burst} TFLOP/s x {BF16_TO_FP4:g} (FP4/BF16 nominal)",
+                     "traffic": gemm_traffic(sha),
+                     "frac_of_9pf": round(gemm_tflops / (PAGES_FP4_PF * 1000), 4),
+                     "frac_of_13p5pf": round(gemm_tflops / (NOMINAL_FP4_PF * 1000), 4)},
+        "kernels_ms": {"quantize_x_row_col": round(float(t_qx.mean()), 5),
+                       "quantize_w": round(float(t_qw.mean()), 5),
+                       "gemm": round(float(t_gemm.mean()), 5)},
+        "quantize": {"x_row_col_gbs": round(qx_gbs, 1), "w_gbs": round(qw_gbs, 1),
+                     "hbm_peak_gbs": hbm_gbs, "x_frac": round(qx_gbs / hbm_gbs, 4),
+                     "w_frac": round(qw_gbs / hbm_gbs, 4), "peak_basis": f"{peak_src} copy bandwidth"},
+        "clocks": clk,
+        "gpu_launches": 4 * args.steps,
+        "wall_s_timed_loop": round(t_wall, 3),
+    }
+    if not args.no_moe:
+        result["moe"] = run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs)
+        result["gpu_launches"] += result["moe"].pop("launches")
+    st = ops.nvfp4_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the run: {ops.STATUS_NAMES.get(st)}")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
+    """The MoE expert step of the Qwen3-30B-A3B workload at 4096 tokens, with
+    expert weights quantized once (they are fixed within a step)."""
+    wl = W.config3()
+    m = wl.moe
+    T, H, F, E, k = m.tokens, m.hidden, m.ffn, m.experts, m.topk
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x = to_dev(m.x)
+    ids = torch.from_numpy(m.topk_ids).to(dev)
+    w1 = ops.quantize_experts(to_dev(m.w1))
+    w2 = ops.quantize_experts(to_dev(m.w2))
+    cap = ops.nvfp4_moe_capacity(T, k, E, 128)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    gather = torch.empty(cap, dtype=torch.int32, device=dev)
+    dst = torch.empty((T, k), dtype=torch.int32, device=dev)
+    pws_b = ops.nvfp4_moe_permute_workspace_bytes(T, k, E)
+    pws = torch.empty(pws_b, dtype=torch.uint8, device=dev)
+    a = dict(rows=cap, cols=H, q=torch.empty((cap, H // 2), dtype=torch.uint8, device=dev),
+             sf=torch.empty(ops.nvfp4_sf_bytes(cap, H), dtype=torch.uint8, device=dev),
+             s=torch.empty(cap, dtype=torch.float32, device=dev))
+    y1 = torch.empty((cap, 2 * F), dtype=torch.bfloat16, device=dev)
+    hq = dict(rows=cap, cols=F, q=torch.empty((cap, F // 2), dtype=torch.uint8, device=dev),
+              sf=torch.empty(ops.nvfp4_sf_bytes(cap, F), dtype=torch.uint8, device=dev),
+              s=torch.empty(cap, dtype=torch.float32, device=dev))
+    y2 = torch.empty((cap, H), dtype=torch.bfloat16, device=dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def step(evs=None):
+        r = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
+        r(0)
+        ops.nvfp4_moe_permute(ids, T, k, E, 128, off, gather, cap, dst, pws, pws_b, stream)
+        r(1)
+        ops.nvfp4_quantize_per_token(x, T, H, H, gather, cap, ops.PER_TOKEN, a["q"], a["sf"], a["s"],
+                                     stream=stream)
+        r(2)
+        ops.nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], cap, off, E, w1["q"], w1["sf"], w1["s"],
+                               2 * F, H, y1, stream)
+        r(3)
+        ops.nvfp4_swiglu_quantize(y1, cap, F, 2 * F, off[E:], hq["q"], hq["sf"], hq["s"], None, stream)
+        r(4)
+        ops.nvfp4_grouped_gemm(hq["q"], hq["sf"], hq["s"], cap, off, E, w2["q"], w2["sf"], w2["s"],
+                               H, F, y2, stream)
+        r(5)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    runs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        evs = [ev() for _ in range(6)]
+        step(evs)
+        runs.append(evs)
+    torch.cuda.synchronize()
+    seg = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in runs]).mean(axis=0)
+    total = float(np.array([e[0].elapsed_time(e[5]) for e in runs]).mean())
+    routed = T * k
+    flop = 2.0 * routed * H * 2 * F + 2.0 * routed * F * H
+    fc1_flop = 2.0 * routed * H * 2 * F
+    fc2_flop = 2.0 * routed * F * H
+    used_rows = int(off[E].item())
+    # weight bytes each grouped GEMM must read at least once (codes + scales + row scales)
+    w1_bytes = E * (2 * F) * (H // 2 + H // 16 + 4)
+    w2_bytes = E * H * (F // 2 + F // 16 + 4)
+    return {
+        "workload": "qwen3_30b_a3b_moe_4096tok_128e_top8 (hidden 2048, expert ffn 768)",
+        "ms_per_step": round(total, 5),
+        "tflops": round(world * flop / (total * 1e-3) / 1e12, 2),
+        "padded_rows": used_rows, "routed_rows": routed,
+        "kernels_ms": {"permute": round(seg[0], 5), "gather_quantize": round(seg[1], 5),
+                       "grouped_fc1": round(seg[2], 5), "swiglu_quantize": round(seg[3], 5),
+                       "grouped_fc2": round(seg[4], 5)},
+        "grouped_fc1": {"tflops": round(fc1_flop / (seg[2] * 1e-3) / 1e12, 1),
+                        "frac_of_fp4_peak": round(fc1_flop / (seg[2] * 1e-3) / 1e12 / fp4_peak, 4),
+                        "weight_gbs": round(w1_bytes / (seg[2] * 1e-3) / 1e9, 1),
+                        "weight_frac_of_hbm": round(w1_bytes / (seg[2] * 1e-3) / 1e9 / hbm_gbs, 4)},
+        "grouped_fc2": {"tflops": round(fc2_flop / (seg[4] * 1e-3) / 1e12, 1),
+                        "frac_of_fp4_peak": round(fc2_flop / (seg[4] * 1e-3) / 1e12 / fp4_peak, 4),
+                        "weight_gbs": round(w2_bytes / (seg[4] * 1e-3) / 1e9, 1),
+                        "weight_frac_of_hbm": round(w2_bytes / (seg[4] * 1e-3) / 1e9 / hbm_gbs, 4)},
+        "launches": 7 * args.steps,
+    }
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timings (baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(wl, rows_x, rows_w, nthreads):
+    """One bounded sample of the step on the oracle: quantize rows_x rows of X
+    and rows_w rows of W, then their exact W4A4 product.  Returns (flop, s)."""
+    import oracle
+    t0 = time.perf_counter()
+    a = oracle.quantize(wl.x[:rows_x], nthreads=nthreads)
+    b = oracle.quantize(wl.w[:rows_w], nthreads=nthreads)
+    oracle.gemm_exact(a, b, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows_x * rows_w * K, dt
+
+
+def cpu_baseline(wl, target_s=12.0):
+    import oracle
+    cores = os.cpu_count() or 1
+    rx, rw = 128, 1024
+    flop, dt = oracle_sample(wl, rx, rw, cores)
+    reps = max(1, int(target_s / max(dt, 1e-3)))
+    tot_f, tot_t = 0.0, 0.0
+    for _ in range(min(reps, 200)):
+        f, t = oracle_sample(wl, rx, rw, cores)
+        tot_f += f
+        tot_t += t
+    return {"value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"quantize {rx} rows of X and {rw} rows of W (per-token), exact int64 W4A4 "
+                      f"product {rx}x{rw}x{K}; {min(reps, 200)} repetitions, {tot_t:.1f} s"}
+
+
+def run_reference(args):
+    from nvfp4_precision_rl_gb300 import workloads as W
+    wl = W.config2()
+    cores = os.cpu_count() or 1
+    rx, rw = 128, 1024
+    for _ in range(args.warmup):
+        oracle_sample(wl, rx, rw, cores)
+    flops, times = 0.0, []
+    for _ in range(args.steps):
+        f, t = oracle_sample(wl, rx, rw, cores)
+        flops = f
+        times.append(t)
+    ms = float(np.mean(times)) * 1e3
+    value = flops / (ms * 1e-3) / 1e12
+    sample = (f"per step: quantize {rx} rows of X and {rw} rows of W (per-token), exact int64 "
+              f"W4A4 product {rx}x{rw}x{K} on {cores} host threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64 exact / f64",
+        "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": WORKLOAD, "M_tokens": M, "N": N, "K": K, "seq_len": 4096,
+                   "micro_batch": 1, "sample_rows_x": rx, "sample_rows_w": rw},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    result = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -16,8 +16,12 @@
 //   warp 1      TMEM allocator + MMA issuer: tcgen05.cp moves the scale tiles
 //               from shared memory to TMEM, tcgen05.mma accumulates the 128 x 256
 //               output tile in TMEM, tcgen05.commit releases ring stages.
-//   warps 2..5  epilogue: tcgen05.ld the accumulator, scale by S_a * S_b,
-//               round to bf16, release the accumulator, store.
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant (128 columns each):
+//               stage S_b in shared memory and load S_a while the tile is still
+//               accumulating, then tcgen05.ld the accumulator 32 columns at a
+//               time (the second warp of the quadrant overlaps the first), scale
+//               by S_a * S_b with packed FP32x2 multiplies, round to bf16,
+//               release the accumulator, store.
 // Tile 128 x 256 x 256 (K step of 256 FP4 = 128 bytes = one swizzle row).
 // The grouped (MoE) variant walks the padded per-expert layout: each 128-row
 // tile belongs to one expert, found from the device-side offsets.
@@ -37,7 +41,8 @@ constexpr int kBN = 256;
 constexpr int kBKBytes = 128;                // 256 FP4 values per K step
 constexpr int kStages = 4;
 constexpr int kMmaPerStage = 4;              // K = 64 per tcgen05.mma
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                 // two per TMEM lane quadrant, 128 columns each
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kATileBytes = kBM * kBKBytes;      // 16 KB
 constexpr uint32_t kBTileBytes = kBN * kBKBytes;      // 32 KB
 constexpr uint32_t kSFAtomBytes = 512;                // 128 rows x 4 scales
@@ -46,8 +51,9 @@ constexpr uint32_t kSFBTileBytes = 8 * kSFAtomBytes;  // 4 KB per stage
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSFTmemCol = 256;                  // after the 256 accumulator columns
 constexpr uint32_t kSFTmemPerStage = 48;              // 16 (A) + 32 (B)
+constexpr uint32_t kSBBytes = kEpiWarps * (kBN / 2) * 4; // per-warp copy of the tile's S_b half
 constexpr size_t kSmemBytes =
-    1024 + kStages * (kATileBytes + kBTileBytes + kSFATileBytes + kSFBTileBytes) + 256;
+    1024 + kStages * (kATileBytes + kBTileBytes + kSFATileBytes + kSFBTileBytes) + kSBBytes + 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;      // 0.2 s
 
@@ -140,6 +146,8 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // 32 lanes x 32 consecutive 32-bit columns; thread t gets lane (base + t).
+// The registers are valid only after tmem_wait() on the same array, which
+// follows immediately.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -151,15 +159,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    // The wait names the registers so no use of them can move above it.
+}
+
+// Wait for this thread's outstanding tcgen05.ld; naming the registers keeps
+// every use of them below the wait.
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.wait::ld.sync.aligned;"
         : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
           "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
           "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
           "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
-          "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-        :: "memory");
+          "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// 32 accumulator columns -> 16 packed bf16 pairs: y = bf16_rn(acc * S_b[n] * S_a).
+__device__ __forceinline__ void scale_chunk(const uint32_t (&r)[32], const float* sb, float sa,
+                                            uint32_t* out) {
+    const float2 sa2 = make_float2(sa, sa);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const float4 b4 = *reinterpret_cast<const float4*>(sb + j);
+        float2 v0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                               make_float2(b4.x, b4.y));
+        float2 v1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                               make_float2(b4.z, b4.w));
+        v0 = __fmul2_rn(v0, sa2);
+        v1 = __fmul2_rn(v1, sa2);
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(v0.x, v0.y);
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(v1.x, v1.y);
+        out[j / 2] = *reinterpret_cast<const uint32_t*>(&h0);
+        out[j / 2 + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -212,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sB = sA + kStages * kATileBytes;
     uint8_t* sSFA = sB + kStages * kBTileBytes;
     uint8_t* sSFB = sSFA + kStages * kSFATileBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + kStages * kSFBTileBytes);
+    float* sSB = reinterpret_cast<float*>(sSFB + kStages * kSFBTileBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sSB) + kSBBytes);
     uint64_t* empty = full + kStages;
     uint64_t* acc_full = empty + kStages;
     uint64_t* acc_empty = acc_full + 1;
@@ -241,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4 * 32);
+        mbar_init(acc_empty, kEpiWarps * 32);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -365,9 +397,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 2) {
         // ------------------------------ epilogue ------------------------------
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const int half = (warp - 2) >> 2;          // which 128 columns of the tile
+        const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
+        float* sb_s = sSB + (warp - 2) * (kBN / 2);
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            // scales first: their loads overlap the tile's main loop
+            const Tile tl = tile_at<kGrouped>(p, t, used_m_tiles);
+            const int64_t m = tl.m0 + quad * 32 + lane;
+            const float sa = (m < p.M) ? __ldg(p.sa + m) : 0.0f;
+            const int64_t n_half = tl.n0 + half * (kBN / 2);
+            const float* sbp = p.sb + (kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half;
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < kBN / 2 / 32; ++i) {
+                const int64_t n = n_half + i * 32 + lane;
+                sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + i * 32 + lane) : 0.0f;
+            }
+            __syncwarp();
             bool ok = mbar_wait_bounded(acc_full, acc_phase, kWaitLimitNs, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) {
@@ -376,34 +423,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const Tile tl = tile_at<kGrouped>(p, t, used_m_tiles);
-            const int64_t m = tl.m0 + quad * 32 + lane;
-            const float sa = (m < p.M) ? __ldg(p.sa + m) : 0.0f;
-            const float* sbp = p.sb + (kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + tl.n0;
-            uint32_t packed[kBN / 2];
+            uint32_t packed[kBN / 4];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
+            for (int c = 0; c < kBN / 64; ++c) {
                 uint32_t r[32];
-                tmem_ld32(t_row + c * 32, r);
-                const int64_t ncol = tl.n0 + c * 32 + lane;
-                const float sbv = (ncol < p.N) ? __ldg(sbp + c * 32 + lane) : 0.0f;
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const float s0 = __fmul_rn(sa, __shfl_sync(0xFFFFFFFFu, sbv, j));
-                    const float s1 = __fmul_rn(sa, __shfl_sync(0xFFFFFFFFu, sbv, j + 1));
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(
-                        __fmul_rn(__uint_as_float(r[j]), s0), __fmul_rn(__uint_as_float(r[j + 1]), s1));
-                    packed[c * 16 + j / 2] = *reinterpret_cast<const uint32_t*>(&h);
-                }
+                tmem_ld32(t_base + c * 32, r);
+                tmem_wait(r);
+                scale_chunk(r, sb_s + c * 32, sa, packed + c * 16);
             }
             tc_fence_before();
             mbar_arrive(acc_empty);
             acc_phase ^= 1u;
             if (m < p.M) {
-                uint16_t* yrow = p.y + m * p.ld_y + tl.n0;
+                uint16_t* yrow = p.y + m * p.ld_y + n_half;
 #pragma unroll
-                for (int v = 0; v < kBN / 8; ++v) {
-                    if (tl.n0 + v * 8 < p.N)
+                for (int v = 0; v < kBN / 2 / 8; ++v) {
+                    if (n_half + v * 8 < p.N)
                         reinterpret_cast<uint4*>(yrow)[v] =
                             make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
                                        packed[4 * v + 3]);

@@ -29,6 +29,7 @@ def assert_quant_equal(gpu, ref, rows=None, what="", col=False):
     rq, rsf, rs = ref[kq], ref[refsf], ref[ks]
     if rows is not None:
         gq, gs = gq[rows], gs[rows]
+        rq, rs = rq[rows], rs[rows]
     bad = np.argwhere(gq != rq)
     assert bad.size == 0, f"{what}: {len(bad)} packed bytes differ, first at {bad[:5].tolist()}"
     assert np.array_equal(gs.view(np.uint32), rs.view(np.uint32)), f"{what}: outer scales differ"
@@ -43,10 +44,19 @@ def bf16_ulp(v):
     return 2.0 ** np.maximum(e - 7, -133)
 
 
+def bf16_floor(y_ref):
+    """Normwise relative error of rounding the exact result itself to bf16."""
+    yr = torch.from_numpy(np.asarray(y_ref, np.float64)).to(torch.bfloat16).double().numpy()
+    den = np.linalg.norm(y_ref)
+    return float(np.linalg.norm(yr - y_ref) / den) if den > 0 else 0.0
+
+
 def check_gemm(y_gpu, y_ref, absy, K, what=""):
-    """GEMM tolerance (reading of the pages' "2e-3 after bf16 rounding"):
-    (i) normwise relative error <= 2e-3; (ii) every element within one bf16 ulp
-    of the exact value plus a 4 * K * 2^-24 FP32-summation allowance."""
+    """GEMM tolerance (reading of the pages' "max relative error 2e-3 after bf16
+    rounding"): (i) normwise relative error <= 2e-3, or, for outputs so small
+    that bf16 rounding of the exact result alone exceeds that (a handful of
+    elements), <= 1.25 x that rounding floor; (ii) every element within one bf16
+    ulp of the exact value plus a 4 * K * 2^-24 FP32-summation allowance."""
     y_gpu = np.asarray(y_gpu, np.float64)
     err = np.abs(y_gpu - y_ref)
     bound = bf16_ulp(y_ref) + 4.0 * K * 2.0 ** -24 * absy
@@ -56,5 +66,6 @@ def check_gemm(y_gpu, y_ref, absy, K, what=""):
     den = np.linalg.norm(y_ref)
     if den > 0:
         rel = np.linalg.norm(y_gpu - y_ref) / den
-        assert rel <= 2e-3, f"{what}: normwise relative error {rel:.3e}"
+        gate = max(2e-3, 1.25 * bf16_floor(y_ref))
+        assert rel <= gate, f"{what}: normwise relative error {rel:.3e} > {gate:.3e}"
     return float(np.max(err / np.maximum(np.abs(y_ref), 1e-30))) if y_ref.size else 0.0
