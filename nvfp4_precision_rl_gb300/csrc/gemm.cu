@@ -13,10 +13,15 @@
 // One persistent CTA per SM, warp-specialised:
 //   warp 0      TMA producer: A/B tiles (cp.async.bulk.tensor, 128B swizzle) and
 //               the swizzled scale tiles (cp.async.bulk) into a 4-stage ring.
-//   warp 1      TMEM allocator + MMA issuer: tcgen05.cp moves the scale tiles
-//               from shared memory to TMEM, tcgen05.mma accumulates the 128 x 256
+//   warp 1      TMEM allocator + MMA issuer: tcgen05.mma accumulates the 128 x 256
 //               output tile in TMEM, tcgen05.commit releases ring stages.
-//   warps 2..9  epilogue, two warps per TMEM lane quadrant (128 columns each):
+//   warps 2..5  scale warps, one per TMEM lane quadrant: each reads the stage's
+//               512-byte scale atoms from shared memory (line = lane) and writes
+//               them into its own 32 TMEM lanes with tcgen05.st -- the same
+//               4-way replicated image a tcgen05.cp 32x128b.warpx4 would make,
+//               but on the warps' TMEM store path, which (measured) overlaps the
+//               MMAs, whereas every tcgen05.cp occupies the serial MMA pipe.
+//   warps 6..13 epilogue, two warps per TMEM lane quadrant (128 columns each):
 //               stage S_b in shared memory and load S_a while the tile is still
 //               accumulating, then tcgen05.ld the accumulator 32 columns at a
 //               time (the second warp of the quadrant overlaps the first), scale
@@ -29,6 +34,8 @@
 // Every wait is bounded: a wait that runs out sets the status word and a shared
 // abort flag, every role leaves its loop, the producer waits (bounded) for its
 // copies in flight, the MMA thread for its tensor-core work, and TMEM is freed.
+// (The scale warps' tcgen05.st are complete before they signal, so they leave
+// nothing in flight.)
 #include <cuda.h>
 
 #include "common.cuh"
@@ -41,8 +48,11 @@ constexpr int kBN = 256;
 constexpr int kBKBytes = 128;                // 256 FP4 values per K step
 constexpr int kStages = 4;
 constexpr int kMmaPerStage = 4;              // K = 64 per tcgen05.mma
+constexpr int kSFWarps = 4;                  // one per TMEM lane quadrant
 constexpr int kEpiWarps = 8;                 // two per TMEM lane quadrant, 128 columns each
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kFirstSFWarp = 2;
+constexpr int kFirstEpiWarp = kFirstSFWarp + kSFWarps;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr uint32_t kATileBytes = kBM * kBKBytes;      // 16 KB
 constexpr uint32_t kBTileBytes = kBN * kBKBytes;      // 32 KB
 constexpr uint32_t kSFAtomBytes = 512;                // 128 rows x 4 scales
@@ -121,18 +131,6 @@ __device__ __forceinline__ uint64_t sw128_desc(const void* p) {
            (2ull << 61);
 }
 
-// Descriptor of one 512-byte scale atom (32 rows of 16 bytes, no swizzle,
-// 8-row core matrices 128 bytes apart) for tcgen05.cp.
-__device__ __forceinline__ uint64_t sf_desc(const void* p) {
-    const uint64_t addr = smem_u32(p);
-    return ((addr >> 4) & 0x3FFFull) | ((128ull >> 4) << 32) | (1ull << 46);
-}
-
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t accumulate, uint32_t sfa_tmem, uint32_t sfb_tmem) {
     asm volatile(
@@ -171,6 +169,34 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[32]) {
           "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
           "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
           "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// Write 16 / 32 consecutive TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+          "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+          "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+          "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+          "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]),
+          "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+          "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 32 accumulator columns -> 16 packed bf16 pairs: y = bf16_rn(acc * S_b[n] * S_a).
@@ -246,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sSB = reinterpret_cast<float*>(sSFB + kStages * kSFBTileBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sSB) + kSBBytes);
     uint64_t* empty = full + kStages;
-    uint64_t* acc_full = empty + kStages;
+    uint64_t* sf_ready = empty + kStages;
+    uint64_t* acc_full = sf_ready + kStages;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* drain = acc_empty + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -271,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], kSFWarps);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kEpiWarps * 32);
@@ -356,20 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
+                // the scale warps have seen the stage full and put its scales in TMEM
+                if (!mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
                 const uint32_t sf_col = tmem + kSFTmemCol + stage * kSFTmemPerStage;
-                const uint8_t* sfa_s = sSFA + stage * kSFATileBytes;
-                const uint8_t* sfb_s = sSFB + stage * kSFBTileBytes;
-                for (int j = 0; j < ng; ++j) {
-                    tc_cp_sf(sf_col + j * 4, sf_desc(sfa_s + j * kSFAtomBytes));
-                    tc_cp_sf(sf_col + 16 + j * 8, sf_desc(sfb_s + j * kSFAtomBytes));
-                    tc_cp_sf(sf_col + 16 + j * 8 + 4, sf_desc(sfb_s + kSFATileBytes + j * kSFAtomBytes));
-                }
                 const uint8_t* a_s = sA + stage * kATileBytes;
                 const uint8_t* b_s = sB + stage * kBTileBytes;
                 for (int j = 0; j < ng; ++j) {
@@ -394,12 +416,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(drain);
         if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr))
             record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
-    } else if (warp >= 2) {
+    } else if (warp >= kFirstSFWarp && warp < kFirstEpiWarp) {
+        // ------------------------------ scale warps ---------------------------
+        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
+                got = __all_sync(0xFFFFFFFFu, got);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                // line `lane` of every 512-byte atom = 16 bytes = 4 TMEM columns
+                const uint4* sfa_s = reinterpret_cast<const uint4*>(sSFA + stage * kSFATileBytes);
+                const uint4* sfb_s = reinterpret_cast<const uint4*>(sSFB + stage * kSFBTileBytes);
+                uint32_t va[16], vb[32];
+#pragma unroll
+                for (int j = 0; j < kMmaPerStage; ++j) {
+                    const uint4 a = (j < ng) ? sfa_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 b0 = (j < ng) ? sfb_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 b1 = (j < ng) ? sfb_s[(kSFATileBytes / 16) + j * 32 + lane]
+                                              : make_uint4(0u, 0u, 0u, 0u);
+                    va[4 * j] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
+                    vb[8 * j] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
+                    vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z;
+                    vb[8 * j + 7] = b1.w;
+                }
+                const uint32_t sf_col = tmem + t_lane + kSFTmemCol + stage * kSFTmemPerStage;
+                tmem_st16(sf_col, va);
+                tmem_st32(sf_col + 16, vb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_ready[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
+        }
+    } else if (warp >= kFirstEpiWarp) {
         // ------------------------------ epilogue ------------------------------
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const int half = (warp - 2) >> 2;          // which 128 columns of the tile
+        const int half = (warp - kFirstEpiWarp) >> 2;   // which 128 columns of the tile
         const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
-        float* sb_s = sSB + (warp - 2) * (kBN / 2);
+        float* sb_s = sSB + (warp - kFirstEpiWarp) * (kBN / 2);
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             // scales first: their loads overlap the tile's main loop
