@@ -59,6 +59,22 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value, device, world):
+    """Largest value of a per-rank float across ranks (the step time the job sees)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, seconds_max):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -236,13 +252,9 @@ def run_ours(args, rank, world, local_rank):
     t_qw = np.array([e[1].elapsed_time(e[2]) for e in steps_ev])
     t_gemm = np.array([e[2].elapsed_time(e[3]) for e in steps_ev])
     ms_step = float(t_step.mean())
-    ms_step_max = ms_step
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step_max = float(tt.item())
+    ms_step_max = max_over_ranks(ms_step, dev, world)
     flop = 2.0 * M * N * K
-    value = world * flop / (ms_step_max * 1e-3) / 1e12
+    value = job_throughput(flop, world, ms_step_max * 1e-3) / 1e12
 
     # ---- end to end through the library calls with host buffers ----
     x_host = torch.from_numpy(wl.x.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -262,12 +274,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step = float(np.mean(e2e_ms))
-    if world > 1:
-        tt = torch.tensor([e2e_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_step = float(tt.item())
-    e2e_value = world * flop / (e2e_step * 1e-3) / 1e12
+    e2e_step = max_over_ranks(float(np.mean(e2e_ms)), dev, world)
+    e2e_value = job_throughput(flop, world, e2e_step * 1e-3) / 1e12
 
     hbm_gbs, bf16_burst, bf16_sust, peak_src = measured_peaks()
     fp4_peak = bf16_burst * BF16_TO_FP4
