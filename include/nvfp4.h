@@ -190,6 +190,33 @@ NVFP4_API nvfp4_status nvfp4_moe_permute(
     int32_t row_align, int32_t* expert_offsets, int32_t* gather_rows, int64_t capacity,
     int32_t* dst_rows, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_moe_permute for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers that
+ * cannot call cudaMalloc (or any allocating routine) where they route tokens:
+ * code running while a CUDA graph is captured, runtimes whose device memory is
+ * owned by another allocator, or decode loops that forbid allocation on the hot
+ * path.  It computes exactly what nvfp4_moe_permute computes, with the same
+ * arguments minus the workspace: the per-chunk histogram scratch lives in a
+ * fixed 1 MiB __device__ array inside this library, which every device that
+ * loads the library holds until the process exits.
+ *
+ *  Limit: nvfp4_moe_permute_workspace_bytes(tokens, topk, num_experts) must be
+ *  <= 1 MiB (for 128 experts: up to 2,097,152 routed (token, slot) pairs);
+ *  larger sizes return NVFP4_ERR_WORKSPACE and launch nothing.
+ *  The first call on a device looks up the array's device address (with that
+ *  device current) and so should come before any stream capture.
+ *  Nothing in the array needs to start at zero (every histogram entry read is
+ *  first written by the same call), but every call shares it: calls that
+ *  overlap on the GPU (other streams, other host threads) race and must be
+ *  serialised by the caller.  Nothing is allocated or freed by this call.
+ */
+NVFP4_API nvfp4_status nvfp4_moe_permute_noalloc(
+    const int32_t* topk_ids, int64_t tokens, int32_t topk, int32_t num_experts,
+    int32_t row_align, int32_t* expert_offsets, int32_t* gather_rows, int64_t capacity,
+    int32_t* dst_rows, nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Block-scaled W4A4 GEMMs                                                   */
 /* ------------------------------------------------------------------------- */

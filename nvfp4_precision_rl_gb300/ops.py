@@ -55,6 +55,7 @@ def lib():
         "nvfp4_moe_capacity": (I64, [I64, I32, I32, I32]),
         "nvfp4_moe_permute_workspace_bytes": (SZ, [I64, I32, I32]),
         "nvfp4_moe_permute": (st, [P, I64, I32, I32, I32, P, P, I64, P, P, SZ, P]),
+        "nvfp4_moe_permute_noalloc": (st, [P, I64, I32, I32, I32, P, P, I64, P, P]),
         "nvfp4_gemm": (st, [P, P, P, I64, P, P, P, I64, I64, P, I64, P]),
         "nvfp4_grouped_gemm": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
         "nvfp4_swiglu_quantize": (st, [P, I64, I64, I64, P, P, P, P, P, P]),
@@ -125,6 +126,15 @@ def nvfp4_moe_permute(topk_ids, tokens, topk, num_experts, row_align, expert_off
     _ok("nvfp4_moe_permute", lib().nvfp4_moe_permute(
         _p(topk_ids), tokens, topk, num_experts, row_align, _p(expert_offsets), _p(gather_rows),
         capacity, _p(dst_rows), _p(workspace), workspace_bytes, _s(stream)))
+
+
+def nvfp4_moe_permute_noalloc(topk_ids, tokens, topk, num_experts, row_align, expert_offsets,
+                              gather_rows, capacity, dst_rows, stream=None):
+    """nvfp4_moe_permute without a caller workspace (for callers that cannot
+    allocate): the library's fixed 1 MiB scratch array is used instead."""
+    _ok("nvfp4_moe_permute_noalloc", lib().nvfp4_moe_permute_noalloc(
+        _p(topk_ids), tokens, topk, num_experts, row_align, _p(expert_offsets), _p(gather_rows),
+        capacity, _p(dst_rows), _s(stream)))
 
 
 def nvfp4_gemm(a_q, a_sf, a_s, M, b_q, b_sf, b_s, N, K, y, ld_y, stream=None):
