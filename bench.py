@@ -75,6 +75,18 @@ def job_throughput(units_per_rank, world, seconds_max):
     return units_per_rank * world / seconds_max
 
 
+def capture_graphs(torch, stages, stream):
+    """One CUDA graph per stage of the step (captured after the eager warm-up)."""
+    graphs = []
+    for fn in stages:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    return graphs
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -170,7 +182,10 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    stream = torch.cuda.current_stream()
+    # one side stream for everything: the library calls are stream-ordered and
+    # allocation-free, so each stage is captured once into a CUDA graph and replayed
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
 
     def to_dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -208,26 +223,29 @@ def run_ours(args, rank, world, local_rank):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        quant_x(x)
-        if evs:
-            evs[1].record(stream)
-        quant_w()
-        if evs:
-            evs[2].record(stream)
-        gemm()
-        if evs:
-            evs[3].record(stream)
-
+    stages = [lambda: quant_x(x), quant_w, gemm]
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        step()
+        for fn in stages:
+            fn()
     torch.cuda.synchronize()
     st = ops.nvfp4_get_device_status()
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {ops.STATUS_NAMES.get(st)}")
+    graphs = capture_graphs(torch, stages, stream)
+
+    def step(evs=None):
+        for i, g in enumerate(graphs):
+            if evs:
+                evs[i].record(stream)
+            g.replay()
+        if evs:
+            evs[len(graphs)].record(stream)
+
+    for _ in range(2):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
 
     clocks = Clocks(local_rank)
     if world > 1:
@@ -297,7 +315,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "M_tokens": M, "N": N, "K": K, "seq_len": 4096,
                    "micro_batch": 1, "column_copy": True, "scale_mode": "per_token",
                    "parallelism": f"dp{world} (independent batches, no collective)",
-                   "l2": "flushed (512 MB write) before every timed step"},
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "launch": "each stage captured once as a CUDA graph and replayed"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(M * K * 2), "d2h_bytes_per_step": int(M * N * 2),
                 "ms_per_step": round(e2e_step, 5)},
@@ -363,27 +382,32 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    def step(evs=None):
-        r = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
-        r(0)
-        ops.nvfp4_moe_permute(ids, T, k, E, 128, off, gather, cap, dst, pws, pws_b, stream)
-        r(1)
-        ops.nvfp4_quantize_per_token(x, T, H, H, gather, cap, ops.PER_TOKEN, a["q"], a["sf"], a["s"],
-                                     stream=stream)
-        r(2)
-        ops.nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], cap, off, E, w1["q"], w1["sf"], w1["s"],
-                               2 * F, H, y1, stream)
-        r(3)
-        ops.nvfp4_swiglu_quantize(y1, cap, F, 2 * F, off[E:], hq["q"], hq["sf"], hq["s"], None, stream)
-        r(4)
-        ops.nvfp4_grouped_gemm(hq["q"], hq["sf"], hq["s"], cap, off, E, w2["q"], w2["sf"], w2["s"],
-                               H, F, y2, stream)
-        r(5)
-
+    stages = [
+        lambda: ops.nvfp4_moe_permute(ids, T, k, E, 128, off, gather, cap, dst, pws, pws_b, stream),
+        lambda: ops.nvfp4_quantize_per_token(x, T, H, H, gather, cap, ops.PER_TOKEN, a["q"], a["sf"],
+                                             a["s"], stream=stream),
+        lambda: ops.nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], cap, off, E, w1["q"], w1["sf"],
+                                       w1["s"], 2 * F, H, y1, stream),
+        lambda: ops.nvfp4_swiglu_quantize(y1, cap, F, 2 * F, off[E:], hq["q"], hq["sf"], hq["s"], None,
+                                          stream),
+        lambda: ops.nvfp4_grouped_gemm(hq["q"], hq["sf"], hq["s"], cap, off, E, w2["q"], w2["sf"],
+                                       w2["s"], H, F, y2, stream),
+    ]
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        step()
+        for fn in stages:
+            fn()
     torch.cuda.synchronize()
+    graphs = capture_graphs(torch, stages, stream)
+
+    def step(evs=None):
+        for i, g in enumerate(graphs):
+            if evs:
+                evs[i].record(stream)
+            g.replay()
+        if evs:
+            evs[len(graphs)].record(stream)
+
     runs = []
     for _ in range(args.steps):
         flush.zero_()

@@ -79,6 +79,113 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(RowParams p) {
         atomicMax(p.amax_ws, __float_as_uint(seen_amax));
 }
 
+// Rows staged through shared memory by bulk TMA copies: persistent CTAs, each
+// warp owns `depth` row buffers and keeps up to `depth` rows of its grid-stride
+// sequence in flight (one cp.async.bulk per row, completion on a per-buffer
+// mbarrier), so memory-level parallelism no longer depends on how many rows fit
+// in registers.  The per-row arithmetic is the register kernel's (rowquant.cuh).
+struct StageCfg {
+    int depth;          // row buffers per warp
+    uint32_t row_pad;   // bytes per row buffer (row bytes rounded up to 128)
+};
+
+__device__ __forceinline__ void bulk_row_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <int NB, int MODE>
+__global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowParams p, StageCfg cfg) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    uint8_t* bufs = smem + static_cast<size_t>(warp) * cfg.depth * cfg.row_pad;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(nwarps) * cfg.depth * cfg.row_pad) +
+                     warp * cfg.depth;
+    const int nblocks = p.cols >> 4;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.cols) * 2u;
+    const float tensor_amax = (MODE == kPerTensor) ? __uint_as_float(*p.amax_ws) : 0.0f;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+
+    if (lane == 0) {
+        for (int d = 0; d < cfg.depth; ++d) mbar_init(&bars[d], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // Start the copy of row r into buffer d (a zero row only completes the phase).
+    auto issue = [&](int64_t r, int d) {
+        if (r >= p.rows_out || lane != 0) return;
+        const int64_t src = source_row(p, r);
+        if (src >= 0) {
+            mbar_arrive_expect_tx(&bars[d], row_bytes);
+            bulk_row_load(bufs + static_cast<size_t>(d) * cfg.row_pad, p.x + src * p.ld_x, row_bytes,
+                          &bars[d]);
+        } else {
+            mbar_arrive(&bars[d]);
+        }
+    };
+    for (int d = 0; d < cfg.depth; ++d) issue(first + d * stride, d);
+
+    float seen_amax = 0.0f;
+    uint32_t parity = 0;   // bit d = phase parity expected next on buffer d
+    int d = 0;
+    for (int64_t r = first; r < p.rows_out; r += stride) {
+        const int64_t src = p.gather ? static_cast<int64_t>(p.gather[r]) : r;
+        const bool zero_row = src < 0 || src >= p.rows_in;   // no copy was issued for it
+        bool ok = mbar_wait_bounded(&bars[d], (parity >> d) & 1u, 2000000000ull, nullptr);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_NONE);
+                // let the copies this warp still has in flight land before it exits
+                for (int k = 0; k < cfg.depth; ++k) {
+                    const int bb = (d + k) % cfg.depth;
+                    if (r + k * stride < p.rows_out)
+                        mbar_wait_bounded(&bars[bb], (parity >> bb) & 1u, 200000000ull, nullptr);
+                }
+            }
+            break;
+        }
+        parity ^= 1u << d;
+        const uint4* row = reinterpret_cast<const uint4*>(bufs + static_cast<size_t>(d) * cfg.row_pad);
+        Block16 v[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int b = i * 32 + lane;
+            const bool in = !zero_row && b < nblocks;
+            v[i].lo = in ? row[2 * b] : make_uint4(0u, 0u, 0u, 0u);
+            v[i].hi = in ? row[2 * b + 1] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();                       // every lane has read the buffer
+        issue(r + cfg.depth * stride, d);   // refill it with the row `depth` steps ahead
+        d = (d + 1 == cfg.depth) ? 0 : d + 1;
+        float bmax[NB];
+        float row_amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            bmax[i] = block_absmax(v[i]);
+            row_amax = fmaxf(row_amax, bmax[i]);
+        }
+        row_amax = warp_max(row_amax);
+        seen_amax = fmaxf(seen_amax, row_amax);
+        if (MODE == kAmaxOnly) continue;
+        encode_row_blocks<NB>(v, bmax, MODE == kPerTensor ? tensor_amax : row_amax, nblocks, p.kgroups,
+                              reinterpret_cast<uint2*>(p.q), p.sf, p.s, r, lane);
+    }
+    if (MODE != kAmaxOnly) {
+        // padding rows of the swizzled scales (rows_out .. rows_pad)
+        for (int64_t rp = p.rows_out + first; rp < p.rows_pad; rp += stride)
+            zero_sf_row(p.sf, p.kgroups, rp, lane);
+    }
+    if (MODE != kPerTensor && p.amax_ws != nullptr && lane == 0 && seen_amax > 0.0f)
+        atomicMax(p.amax_ws, __float_as_uint(seen_amax));
+}
+
 // Rows longer than 256 * 16 elements: two passes over the row (the second from L1/L2).
 template <int MODE>
 __global__ void __launch_bounds__(kRowThreads) quant_rows_long_kernel(RowParams p) {
@@ -215,9 +322,55 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
     *reinterpret_cast<uint32_t*>(p.sf + sf_word_offset(k0 + 1, g, p.kgroups)) = col_ok ? word1 : 0u;
 }
 
+// Staged-kernel geometry: as many warps x row buffers as fit in ~200 KB.
+bool staged_config(int cols, int* warps, StageCfg* cfg) {
+    const uint32_t pad = static_cast<uint32_t>(round_up(static_cast<int64_t>(cols) * 2, 128));
+    const size_t budget = 200 * 1024;
+    const int choices[5][2] = {{16, 3}, {16, 2}, {12, 2}, {8, 3}, {8, 2}};
+    for (const auto& c : choices) {
+        if (static_cast<size_t>(c[0]) * c[1] * (pad + 8) <= budget) {
+            *warps = c[0];
+            cfg->depth = c[1];
+            cfg->row_pad = pad;
+            return true;
+        }
+    }
+    return false;
+}
+
+template <int NB, int MODE>
+nvfp4_status launch_staged(const RowParams& p, int warps, StageCfg cfg, const DeviceCtx& ctx,
+                           cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(warps) * cfg.depth * (cfg.row_pad + 8);
+    static bool attr[64] = {};
+    if (!attr[ctx.device & 63]) {
+        if (cudaFuncSetAttribute(quant_rows_staged_kernel<NB, MODE>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        attr[ctx.device & 63] = true;
+    }
+    const int64_t rows = (MODE == kAmaxOnly) ? p.rows_out : p.rows_pad;
+    const int64_t want = ceil_div(rows, warps);
+    const int grid = static_cast<int>(want < ctx.sm_count ? want : ctx.sm_count);
+    quant_rows_staged_kernel<NB, MODE><<<grid, warps * 32, smem, s>>>(p, cfg);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
+}
+
 template <int MODE>
-nvfp4_status launch_rows(const RowParams& p, int blocks, cudaStream_t s) {
+nvfp4_status launch_rows(const RowParams& p, int blocks, const DeviceCtx& ctx, cudaStream_t s) {
     const int need = (p.cols / 8 + 31) / 32;
+    int warps = 0;
+    StageCfg cfg{0, 0};
+    const int nb = (p.cols / 16 + 31) / 32;   // 16-element blocks per lane
+    if (nb <= 8 && staged_config(p.cols, &warps, &cfg)) {
+        if (nb <= 1) return launch_staged<1, MODE>(p, warps, cfg, ctx, s);
+        if (nb <= 2) return launch_staged<2, MODE>(p, warps, cfg, ctx, s);
+        if (nb <= 3) return launch_staged<3, MODE>(p, warps, cfg, ctx, s);
+        if (nb <= 4) return launch_staged<4, MODE>(p, warps, cfg, ctx, s);
+        if (nb <= 6) return launch_staged<6, MODE>(p, warps, cfg, ctx, s);
+        return launch_staged<8, MODE>(p, warps, cfg, ctx, s);
+    }
     if (need <= 1) quant_rows_kernel<1, MODE><<<blocks, kRowThreads, 0, s>>>(p);
     else if (need <= 2) quant_rows_kernel<2, MODE><<<blocks, kRowThreads, 0, s>>>(p);
     else if (need <= 4) quant_rows_kernel<4, MODE><<<blocks, kRowThreads, 0, s>>>(p);
@@ -254,9 +407,9 @@ nvfp4_status quantize_rows_launch(const uint16_t* x, int64_t rows_in, int64_t co
     if (rows_launch == 0) return NVFP4_OK;
     const int64_t want = ceil_div(rows_launch, kRowThreads / 32);
     const int blocks = static_cast<int>(want < 1048576 ? want : 1048576);
-    if (mode == kPerToken) return launch_rows<kPerToken>(p, blocks, stream);
-    if (mode == kPerTensor) return launch_rows<kPerTensor>(p, blocks, stream);
-    return launch_rows<kAmaxOnly>(p, blocks, stream);
+    if (mode == kPerToken) return launch_rows<kPerToken>(p, blocks, ctx, stream);
+    if (mode == kPerTensor) return launch_rows<kPerTensor>(p, blocks, ctx, stream);
+    return launch_rows<kAmaxOnly>(p, blocks, ctx, stream);
 }
 
 nvfp4_status quantize_cols_launch(const uint16_t* x, int64_t rows_in, int64_t cols, int64_t ld_x,

@@ -100,4 +100,62 @@ __device__ __forceinline__ void encode_row(const uint4 (&v)[NCH], const float (&
     if (lane == 0) s[r] = rec.S;
 }
 
+// ---------------------------------------------------------------------------
+// Block-per-lane variant: lane l owns 16-element blocks l, l+32, ... of a row
+// (32 contiguous bytes each, read from shared memory), so the block scale is
+// computed once per block and the 16 multiplies run as 8 packed FP32x2 ops.
+// ---------------------------------------------------------------------------
+struct Block16 {
+    uint4 lo, hi;   // elements 0..7 and 8..15 of the block (bf16 pairs)
+};
+
+__device__ __forceinline__ float block_absmax(const Block16& b) {
+    const uint32_t m = bmax2(bmax2(bmax2(b.lo.x & kAbsMask2, b.lo.y & kAbsMask2),
+                                   bmax2(b.lo.z & kAbsMask2, b.lo.w & kAbsMask2)),
+                             bmax2(bmax2(b.hi.x & kAbsMask2, b.hi.y & kAbsMask2),
+                                   bmax2(b.hi.z & kAbsMask2, b.hi.w & kAbsMask2)));
+    return fmaxf(bf16lo(m), bf16hi(m));
+}
+
+// x * r for the two bf16 values of a word (correctly rounded, like __fmul_rn).
+__device__ __forceinline__ float2 scale_pair(uint32_t w, float2 r2) {
+    return __fmul2_rn(make_float2(bf16lo(w), bf16hi(w)), r2);
+}
+
+__device__ __forceinline__ uint32_t encode8(const uint4& v, float2 r2) {
+    const float2 a = scale_pair(v.x, r2), b = scale_pair(v.y, r2);
+    const float2 c = scale_pair(v.z, r2), d = scale_pair(v.w, r2);
+    return cvt_e2m1x8(a.x, a.y, b.x, b.y, c.x, c.y, d.x, d.y);
+}
+
+// Encode a row whose blocks sit in registers (NB blocks per lane, block
+// b = i * 32 + lane): codes, scale words and the outer scale of row r.
+template <int NB>
+__device__ __forceinline__ void encode_row_blocks(const Block16 (&v)[NB], const float (&bmax)[NB],
+                                                  float amax, int nblocks, int kgroups, uint2* q,
+                                                  uint8_t* sf, float* s, int64_t r, int lane) {
+    const ScaleRecipe rec(amax);
+    uint2* qrow = q + r * nblocks;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        const int b = i * 32 + lane;
+        float rb;
+        const uint32_t sb = rec.block(bmax[i], &rb);
+        const float2 r2 = make_float2(rb, rb);
+        const uint2 w = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
+        if (b < nblocks) qrow[b] = w;
+        // four consecutive blocks = four consecutive lanes -> one scale word
+        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+        if ((lane & 3) == 0) {
+            const int g = b >> 2;
+            if (g < kgroups)
+                *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, g, kgroups)) =
+                    sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        }
+    }
+    if (lane == 0) s[r] = rec.S;
+}
+
 }  // namespace nvfp4
