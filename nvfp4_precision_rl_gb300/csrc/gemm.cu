@@ -219,6 +219,34 @@ __device__ __forceinline__ void scale_chunk(const uint32_t (&r)[32], const float
     }
 }
 
+// Keeps the compiler from reading `r` before the preceding tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                   "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                   "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                   "+r"(r[31]));
+}
+
+// TMA store of one box of Y from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory source of every committed store has been read
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed store has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------
 // Tile schedule (identical in every role)
 // ----------------------------------------------------------------------------
@@ -526,6 +554,407 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// Dense GEMM on CTA pairs (tcgen05 cta_group::2)
+// ----------------------------------------------------------------------------
+// A cluster of two CTAs on two SMs computes one 256 x 256 output tile with
+// M = 256 MMAs issued by the even CTA: each CTA stages its own 128 rows of A and
+// one 128-row half of the B tile, so per SM each 256-deep K step moves 32 KB of
+// operands into shared memory instead of 48 KB, and the tensor core reads the
+// peer's B half from the peer SM.  Each CTA keeps its 128 x 256 FP32 accumulator
+// and the scale factors of its own MMA rows (A) and of all 256 B rows in its own
+// TMEM, written by its own scale warps.  Cross-CTA signals:
+//   scale warps (both CTAs) -> sf_ready of the even CTA (remote mbarrier arrive),
+//   MMA commits            -> empty / acc_full of both CTAs (multicast commit),
+//   epilogue (both CTAs)   -> acc_empty of the even CTA (remote arrive).
+constexpr int kPStages = 5;
+constexpr uint32_t kPBHalfBytes = 128 * kBKBytes;                 // 16 KB
+// Output staging: per epilogue warp one 32-row x 64-column bf16 box (4 KB),
+// 128-byte swizzled so the tensor-map store reads it back in rows.
+constexpr uint32_t kPOutBoxBytes = 32 * 128;
+constexpr uint32_t kPOutBytes = kEpiWarps * kPOutBoxBytes;        // 32 KB
+constexpr uint32_t kPCarveBytes = kPStages * (kATileBytes + kPBHalfBytes + kSFATileBytes + kSFBTileBytes) +
+                                  kPOutBytes + kSBBytes + 256;
+constexpr size_t kPSmemBytes = 232448;                            // the opt-in maximum (227 KB)
+static_assert(kPCarveBytes + 512 <= kPSmemBytes, "shared memory carve-up");
+// M = 256 across the pair (M >> 4 at bit 24), N = 256.
+constexpr uint32_t kPInstrDesc = (1u << 7) | (1u << 10) | ((256u >> 3) << 17) | ((256u >> 4) << 24);
+static_assert(kSFTmemCol + kPStages * kSFTmemPerStage <= kTmemCols, "TMEM columns");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same object in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
+    return out;
+}
+
+// Arrive on a barrier named by its shared::cluster address (possibly the peer's).
+// Default (CTA-scope release) semantics: what the arrival publishes is either
+// tcgen05 work already completed by tcgen05.wait, or nothing.  (A cluster-scope
+// release measured about 0.8 us per arrival here and held the scale warps to
+// one stage per microsecond.)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (the arrivals come from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                  volatile int* abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+// arrive on the barrier at this offset in both CTAs of the pair
+__device__ __forceinline__ void tc_commit_pair_both(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t accumulate, uint32_t sfa_tmem, uint32_t sfb_tmem) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kPInstrDesc), "r"(accumulate), "r"(sfa_tmem),
+          "r"(sfb_tmem)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
+                           const __grid_constant__ CUtensorMap tma_b,
+                           const __grid_constant__ CUtensorMap tma_y, GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    // the carve-up must fit behind the 1024-byte alignment (uniform in both CTAs)
+    if (static_cast<size_t>(smem - smem_raw) + kPCarveBytes > kPSmemBytes) {
+        if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_UNSUPPORTED_DEVICE, DETAIL_GEMM_DRAIN);
+        return;
+    }
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + kPStages * kATileBytes;
+    uint8_t* sSFA = sB + kPStages * kPBHalfBytes;
+    uint8_t* sSFB = sSFA + kPStages * kSFATileBytes;
+    uint8_t* sOut = sSFB + kPStages * kSFBTileBytes;              // 1024-aligned
+    float* sSB = reinterpret_cast<float*>(sOut + kPOutBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sSB) + kSBBytes);
+    uint64_t* empty = full + kPStages;
+    uint64_t* sf_ready = empty + kPStages;
+    uint64_t* acc_full = sf_ready + kPStages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain = acc_empty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+    const int num_pm = static_cast<int>((p.M + 255) / 256);
+    const int tiles = num_pm * p.num_n_tiles;
+    const int a_row_tiles = static_cast<int>((p.M + 127) / 128);
+    const int sfb_tiles_n = static_cast<int>((p.N + 127) / 128);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 2 * kSFWarps);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 2 * kEpiWarps);     // one arrival per epilogue warp of either CTA
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        // collective across the pair: both CTAs get the same columns
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_holder)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();     // both CTAs' barriers exist before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------ producer (both CTAs) -------------------
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_b)) : "memory");
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued_mask = 0, last_phase = 0;
+        bool ok = true;
+        for (int t = pair; t < tiles && ok; t += npairs) {
+            const int mt = t % num_pm;
+            const int nt = t / num_pm;
+            const int64_t m0 = static_cast<int64_t>(mt) * 256 + rank * 128;
+            const int64_t n0 = static_cast<int64_t>(nt) * kBN;
+            const int a_tile = static_cast<int>(m0 / 128);
+            const bool a_sf_ok = a_tile < a_row_tiles;
+            const int nt128 = static_cast<int>(n0 / 128);
+            const bool two_b_atoms = nt128 + 1 < sfb_tiles_n;
+            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                const uint32_t sf_bytes = ng * kSFAtomBytes;
+                const uint32_t bytes = kATileBytes + kPBHalfBytes + (a_sf_ok ? sf_bytes : 0u) +
+                                       (two_b_atoms ? 2u : 1u) * sf_bytes;
+                mbar_arrive_expect_tx(&full[stage], bytes);
+                tma_load_2d(&tma_a, &full[stage], sA + stage * kATileBytes, kt * kBKBytes,
+                            static_cast<int32_t>(m0));
+                tma_load_2d(&tma_b, &full[stage], sB + stage * kPBHalfBytes, kt * kBKBytes,
+                            static_cast<int32_t>(n0 + rank * 128));
+                const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
+                if (a_sf_ok)
+                    bulk_load(sSFA + stage * kSFATileBytes,
+                              p.sfa + (static_cast<int64_t>(a_tile) * p.kgroups + g0) * kSFAtomBytes,
+                              sf_bytes, &full[stage]);
+                bulk_load(sSFB + stage * kSFBTileBytes,
+                          p.sfb + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
+                          &full[stage]);
+                if (two_b_atoms)
+                    bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
+                              p.sfb + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
+                              sf_bytes, &full[stage]);
+                issued_mask |= 1u << stage;
+                last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
+        }
+        for (int s = 0; s < kPStages; ++s)
+            if (issued_mask & (1u << s))
+                if (!mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kDrainLimitNs, nullptr))
+                    record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------ MMA issuer (even CTA) ------------------
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int t = pair; t < tiles && ok; t += npairs) {
+            if (!mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                // both CTAs' scale warps have seen their stage full and written TMEM
+                if (!mbar_wait_cluster(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                const uint32_t sf_col = tmem + kSFTmemCol + stage * kSFTmemPerStage;
+                const uint8_t* a_s = sA + stage * kATileBytes;
+                const uint8_t* b_s = sB + stage * kPBHalfBytes;
+                for (int j = 0; j < ng; ++j)
+                    tc_mma_pair(tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32),
+                                (kt > 0 || j > 0) ? 1u : 0u, sf_col + j * 4, sf_col + 16 + j * 8);
+                tc_commit_pair_both(&empty[stage]);
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            tc_commit_pair_both(acc_full);
+            acc_phase ^= 1u;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
+        }
+        tc_commit_pair(drain);
+        if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr))
+            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
+    } else if (warp >= kFirstSFWarp && warp < kFirstEpiWarp) {
+        // ------------------------------ scale warps (both CTAs) ----------------
+        const int quad = warp & 3;
+        const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int t = pair; t < tiles && ok; t += npairs) {
+            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
+                got = __all_sync(0xFFFFFFFFu, got);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                const uint4* sfa_s = reinterpret_cast<const uint4*>(sSFA + stage * kSFATileBytes);
+                const uint4* sfb_s = reinterpret_cast<const uint4*>(sSFB + stage * kSFBTileBytes);
+                uint32_t va[16], vb[32];
+#pragma unroll
+                for (int j = 0; j < kMmaPerStage; ++j) {
+                    const uint4 a = (j < ng) ? sfa_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 b0 = (j < ng) ? sfb_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 b1 = (j < ng) ? sfb_s[(kSFATileBytes / 16) + j * 32 + lane]
+                                              : make_uint4(0u, 0u, 0u, 0u);
+                    va[4 * j] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
+                    vb[8 * j] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
+                    vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z;
+                    vb[8 * j + 7] = b1.w;
+                }
+                const uint32_t sf_col = tmem + t_lane + kSFTmemCol + stage * kSFTmemPerStage;
+                tmem_st16(sf_col, va);
+                tmem_st32(sf_col + 16, vb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(peer_addr(&sf_ready[stage], 0));
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
+        }
+    } else if (warp >= kFirstEpiWarp) {
+        // ------------------------------ epilogue (both CTAs) -------------------
+        // Warp (quad, half) owns TMEM lanes quad*32.. and accumulator columns
+        // half*128..: two rounds of 64 columns, each loaded with two tcgen05.ld
+        // and one wait, scaled by S_a[m] S_b[n], rounded to bf16, written into
+        // this warp's swizzled 32 x 64 staging box and stored by TMA (which
+        // clips rows >= M and columns >= N).
+        const int quad = warp & 3;
+        const int ew = warp - kFirstEpiWarp;
+        const int half = ew >> 2;
+        const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
+        float* sb_s = sSB + ew * (kBN / 2);
+        uint8_t* box = sOut + ew * kPOutBoxBytes;
+        uint8_t* my_row = box + lane * 128;
+        const uint32_t acc_empty_leader = peer_addr(acc_empty, 0);
+        uint32_t acc_phase = 0;
+        for (int t = pair; t < tiles; t += npairs) {
+            const int mt = t % num_pm;
+            const int nt = t / num_pm;
+            const int64_t row0 = static_cast<int64_t>(mt) * 256 + rank * 128 + quad * 32;
+            const int64_t m = row0 + lane;
+            const float sa = (m < p.M) ? __ldg(p.sa + m) : 0.0f;
+            const int64_t n_half = static_cast<int64_t>(nt) * kBN + half * (kBN / 2);
+            const float* sbp = p.sb + n_half;
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < kBN / 2 / 32; ++i) {
+                const int64_t n = n_half + i * 32 + lane;
+                sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + i * 32 + lane) : 0.0f;
+            }
+            __syncwarp();
+            bool ok = mbar_wait_cluster(acc_full, acc_phase, kWaitLimitNs, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                *abort_flag = 1;
+                if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int rnd = 0; rnd < 2; ++rnd) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(t_base + rnd * 64, r0);
+                tmem_ld32(t_base + rnd * 64 + 32, r1);
+                tmem_wait(r0);
+                reg_fence(r1);
+                if (rnd == 1) {
+                    // every accumulator read of this tile is complete
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+                }
+                uint32_t q0[16], q1[16];
+                scale_chunk(r0, sb_s + rnd * 64, sa, q0);
+                scale_chunk(r1, sb_s + rnd * 64 + 32, sa, q1);
+                // the previous store from this box has read it
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+                // 16-byte chunk j of row `lane` goes to chunk j ^ (lane % 8) (128-byte swizzle)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(q0[4 * j], q0[4 * j + 1], q0[4 * j + 2], q0[4 * j + 3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(my_row + (((j + 4) ^ (lane & 7)) << 4)) =
+                        make_uint4(q1[4 * j], q1[4 * j + 1], q1[4 * j + 2], q1[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int64_t x = n_half + rnd * 64;
+                if (lane == 0 && row0 < p.M && x < p.N) {
+                    tma_store_2d(&tma_y, box, static_cast<int32_t>(x), static_cast<int32_t>(row0));
+                    bulk_commit();
+                }
+            }
+            acc_phase ^= 1u;
+        }
+        // the staging boxes stay valid until the stores have finished
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();     // the pair's MMAs are done with both CTAs' SMEM and TMEM
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols) : "memory");
+    }
+}
+
+// ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -559,6 +988,19 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_byte
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Y [rows x cols] bf16 with row pitch ld elements; box = 64 columns x 32 rows, 128-byte swizzle.
+bool make_map_y(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool kGrouped>
 nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                          int tiles_upper, const DeviceCtx& ctx, cudaStream_t s) {
@@ -573,6 +1015,38 @@ nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Gem
     const int grid = tiles_upper < ctx.sm_count ? tiles_upper : ctx.sm_count;
     if (grid <= 0) return NVFP4_OK;
     nvfp4_gemm_kernel<kGrouped><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
+}
+
+nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
+                              const GemmParams& p, int64_t pair_tiles, const DeviceCtx& ctx, cudaStream_t s) {
+    static bool attr_set[64] = {};
+    if (!attr_set[ctx.device & 63]) {
+        if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kPSmemBytes)) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        attr_set[ctx.device & 63] = true;
+    }
+    // persistent: as many pairs as can be resident at once (an SM left alone in
+    // its GPC cannot host half of a pair)
+    static int resident[64] = {};
+    if (resident[ctx.device & 63] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ctx.sm_count & ~1), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPSmemBytes;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = ctx.sm_count / 2;
+        }
+        resident[ctx.device & 63] = n;
+    }
+    const int64_t cap = resident[ctx.device & 63];
+    const int64_t pairs = pair_tiles < cap ? pair_tiles : cap;
+    if (pairs <= 0) return NVFP4_OK;
+    nvfp4_gemm_pair_kernel<<<static_cast<int>(2 * pairs), kThreads, kPSmemBytes, s>>>(ma, mb, my, p);
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;
 }
@@ -604,8 +1078,11 @@ nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int
     if (!aligned(a_q, 16) || !aligned(b_q, 16) || !aligned(a_sf, 16) || !aligned(b_sf, 16) ||
         !aligned(y, 16) || !aligned(a_s, 4) || !aligned(b_s, 4))
         return NVFP4_ERR_ALIGNMENT;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, a_q, M, K / 2, kBM) || !make_map(&mb, b_q, N, K / 2, kBN)) return NVFP4_ERR_CUDA;
+    CUtensorMap ma, mb, my;
+    // pairs of CTAs: each loads a 128-row half of the 256-row B tile
+    if (!make_map(&ma, a_q, M, K / 2, kBM) || !make_map(&mb, b_q, N, K / 2, 128) ||
+        !make_map_y(&my, y, M, N, ld_y))
+        return NVFP4_ERR_CUDA;
     GemmParams p;
     p.sfa = static_cast<const uint8_t*>(a_sf);
     p.sfb = static_cast<const uint8_t*>(b_sf);
@@ -623,10 +1100,9 @@ nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int
     p.num_n_tiles = static_cast<int>(ceil_div(N, kBN));
     p.num_m_tiles = static_cast<int>(ceil_div(M, kBM));
     p.E = 0;
-    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
-    if (tiles > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
-    return launch_gemm<false>(ma, mb, p, static_cast<int>(tiles), ctx,
-                              reinterpret_cast<cudaStream_t>(stream));
+    const int64_t pair_tiles = ceil_div(M, 256) * p.num_n_tiles;
+    if (pair_tiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
+    return launch_gemm_pair(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* a_s,
