@@ -320,7 +320,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(M * K * 2), "d2h_bytes_per_step": int(M * N * 2),
                 "ms_per_step": round(e2e_step, 5)},
-        "roofline": {"kernel": "nvfp4_gemm_kernel", "bound": "tensor",
+        "roofline": {"kernel": "nvfp4_gemm_pair_kernel", "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp4_peak, 4),
                      "peak_basis": f"{peak_src} bf16 burst {bf16_burst} TFLOP/s x {BF16_TO_FP4:g} (FP4/BF16 nominal)",

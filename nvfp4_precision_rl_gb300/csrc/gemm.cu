@@ -580,6 +580,14 @@ static_assert(kPCarveBytes + 512 <= kPSmemBytes, "shared memory carve-up");
 constexpr uint32_t kPInstrDesc = (1u << 7) | (1u << 10) | ((256u >> 3) << 17) | ((256u >> 4) << 24);
 static_assert(kSFTmemCol + kPStages * kSFTmemPerStage <= kTmemCols, "TMEM columns");
 
+// true in exactly one active lane of the warp (all lanes must be converged)
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, %1;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+                 : "=r"(pred) : "r"(0xFFFFFFFFu));
+    return pred != 0;
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -775,46 +783,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (issued_mask & (1u << s))
                 if (!mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kDrainLimitNs, nullptr))
                     record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
-    } else if (warp == 1 && lane == 0 && leader) {
+    } else if (warp == 1 && leader) {
         // ------------------------------ MMA issuer (even CTA) ------------------
+        // The whole warp runs the loop (warp-uniform control flow and
+        // descriptors); one elected lane issues the MMAs and commits.
         uint32_t stage = 0, phase = 0, acc_phase = 0;
         bool ok = true;
+        const uint64_t a_desc0 = sw128_desc(sA);
+        const uint64_t b_desc0 = sw128_desc(sB);
         for (int t = pair; t < tiles && ok; t += npairs) {
-            if (!mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                ok = false;
-                break;
-            }
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
+            if (!ok) break;
             tc_fence_after();
             for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                 // both CTAs' scale warps have seen their stage full and written TMEM
-                if (!mbar_wait_cluster(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(0xFFFFFFFFu,
+                                mbar_wait_cluster(&sf_ready[stage], phase, kWaitLimitNs, abort_flag));
+                if (!ok) break;
                 tc_fence_after();
                 const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
                 const uint32_t sf_col = tmem + kSFTmemCol + stage * kSFTmemPerStage;
-                const uint8_t* a_s = sA + stage * kATileBytes;
-                const uint8_t* b_s = sB + stage * kPBHalfBytes;
-                for (int j = 0; j < ng; ++j)
-                    tc_mma_pair(tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32),
-                                (kt > 0 || j > 0) ? 1u : 0u, sf_col + j * 4, sf_col + 16 + j * 8);
-                tc_commit_pair_both(&empty[stage]);
+                // descriptor start addresses advance in 16-byte units: 32 bytes per K step
+                const uint64_t ad = a_desc0 + stage * (kATileBytes >> 4);
+                const uint64_t bd = b_desc0 + stage * (kPBHalfBytes >> 4);
+                if (elect_one()) {
+                    if (ng == kMmaPerStage) {
+#pragma unroll
+                        for (int j = 0; j < kMmaPerStage; ++j)
+                            tc_mma_pair(tmem, ad + 2 * j, bd + 2 * j, (kt > 0 || j > 0) ? 1u : 0u,
+                                        sf_col + j * 4, sf_col + 16 + j * 8);
+                    } else {
+                        for (int j = 0; j < ng; ++j)
+                            tc_mma_pair(tmem, ad + 2 * j, bd + 2 * j, (kt > 0 || j > 0) ? 1u : 0u,
+                                        sf_col + j * 4, sf_col + 16 + j * 8);
+                    }
+                    tc_commit_pair_both(&empty[stage]);
+                }
+                __syncwarp();
                 if (++stage == kPStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            tc_commit_pair_both(acc_full);
+            if (elect_one()) tc_commit_pair_both(acc_full);
+            __syncwarp();
             acc_phase ^= 1u;
         }
         if (!ok) {
             *abort_flag = 1;
-            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
+            if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
         }
-        tc_commit_pair(drain);
-        if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr))
+        // all tensor-core work issued by this warp completes before TMEM is freed
+        if (elect_one()) tc_commit_pair(drain);
+        __syncwarp();
+        if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr) && lane == 0)
             record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
     } else if (warp >= kFirstSFWarp && warp < kFirstEpiWarp) {
         // ------------------------------ scale warps (both CTAs) ----------------
