@@ -567,6 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   MMA commits            -> empty / acc_full of both CTAs (multicast commit),
 //   epilogue (both CTAs)   -> acc_empty of the even CTA (remote arrive).
 constexpr int kPStages = 5;
+constexpr int kPBWarp = kFirstEpiWarp + kEpiWarps;                // the B-side producer
+constexpr int kPThreads = 32 * (kPBWarp + 1);
 constexpr uint32_t kPBHalfBytes = 128 * kBKBytes;                 // 16 KB
 // Output staging: per epilogue warp one 32-row x 64-column bf16 box (4 KB),
 // 128-byte swizzled so the tensor-map store reads it back in rows.
@@ -663,7 +665,7 @@ __device__ __forceinline__ void cluster_sync_all() {
                  ::: "memory");
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                            const __grid_constant__ CUtensorMap tma_b,
                            const __grid_constant__ CUtensorMap tma_y, GemmParams p) {
@@ -703,7 +705,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);               // the A-side and the B-side producer
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 2 * kSFWarps);
         }
@@ -725,10 +727,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------ producer (both CTAs) -------------------
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_a)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_b)) : "memory");
+    if ((warp == 0 || warp == kPBWarp) && lane == 0) {
+        // ------------------------------ producers (both CTAs) ------------------
+        // Two threads in two warps feed each stage: warp 0 loads A and its
+        // scales, warp kPBWarp this CTA's half of B and the B scales.  (TMA
+        // copies issued by one thread complete one after another; two issuing
+        // threads double the rate at which a stage fills.)
+        const bool side_b = warp == kPBWarp;
+        const CUtensorMap* map = side_b ? &tma_b : &tma_a;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
         uint32_t stage = 0, phase = 0;
         uint32_t issued_mask = 0, last_phase = 0;
         bool ok = true;
@@ -748,25 +755,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
                 const uint32_t sf_bytes = ng * kSFAtomBytes;
-                const uint32_t bytes = kATileBytes + kPBHalfBytes + (a_sf_ok ? sf_bytes : 0u) +
-                                       (two_b_atoms ? 2u : 1u) * sf_bytes;
-                mbar_arrive_expect_tx(&full[stage], bytes);
-                tma_load_2d(&tma_a, &full[stage], sA + stage * kATileBytes, kt * kBKBytes,
-                            static_cast<int32_t>(m0));
-                tma_load_2d(&tma_b, &full[stage], sB + stage * kPBHalfBytes, kt * kBKBytes,
-                            static_cast<int32_t>(n0 + rank * 128));
                 const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
-                if (a_sf_ok)
-                    bulk_load(sSFA + stage * kSFATileBytes,
-                              p.sfa + (static_cast<int64_t>(a_tile) * p.kgroups + g0) * kSFAtomBytes,
-                              sf_bytes, &full[stage]);
-                bulk_load(sSFB + stage * kSFBTileBytes,
-                          p.sfb + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
-                          &full[stage]);
-                if (two_b_atoms)
-                    bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
-                              p.sfb + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
-                              sf_bytes, &full[stage]);
+                if (!side_b) {
+                    mbar_arrive_expect_tx(&full[stage], kATileBytes + (a_sf_ok ? sf_bytes : 0u));
+                    tma_load_2d(map, &full[stage], sA + stage * kATileBytes, kt * kBKBytes,
+                                static_cast<int32_t>(m0));
+                    if (a_sf_ok)
+                        bulk_load(sSFA + stage * kSFATileBytes,
+                                  p.sfa + (static_cast<int64_t>(a_tile) * p.kgroups + g0) * kSFAtomBytes,
+                                  sf_bytes, &full[stage]);
+                } else {
+                    mbar_arrive_expect_tx(&full[stage], kPBHalfBytes + (two_b_atoms ? 2u : 1u) * sf_bytes);
+                    tma_load_2d(map, &full[stage], sB + stage * kPBHalfBytes, kt * kBKBytes,
+                                static_cast<int32_t>(n0 + rank * 128));
+                    bulk_load(sSFB + stage * kSFBTileBytes,
+                              p.sfb + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
+                              &full[stage]);
+                    if (two_b_atoms)
+                        bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
+                                  p.sfb + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
+                                  sf_bytes, &full[stage]);
+                }
                 issued_mask |= 1u << stage;
                 last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                 if (++stage == kPStages) {
@@ -779,6 +788,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
             record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
         }
+        // every copy this thread issued must land before the CTA may exit
         for (int s = 0; s < kPStages; ++s)
             if (issued_mask & (1u << s))
                 if (!mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kDrainLimitNs, nullptr))
@@ -885,7 +895,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
             if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
         }
-    } else if (warp >= kFirstEpiWarp) {
+    } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kEpiWarps) {
         // ------------------------------ epilogue (both CTAs) -------------------
         // Warp (quad, half) owns TMEM lanes quad*32.. and accumulator columns
         // half*128..: two rounds of 64 columns, each loaded with two tcgen05.ld
@@ -924,41 +934,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-#pragma unroll
-            for (int rnd = 0; rnd < 2; ++rnd) {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(t_base + rnd * 64, r0);
-                tmem_ld32(t_base + rnd * 64 + 32, r1);
-                tmem_wait(r0);
-                reg_fence(r1);
-                if (rnd == 1) {
-                    // every accumulator read of this tile is complete
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-                }
-                uint32_t q0[16], q1[16];
-                scale_chunk(r0, sb_s + rnd * 64, sa, q0);
-                scale_chunk(r1, sb_s + rnd * 64 + 32, sa, q1);
-                // the previous store from this box has read it
+            // Staging of 64 packed columns (one round): wait until the previous
+            // store from this warp's box has read it, write the rows, then
+            // (separately) fence and store the box with TMA.
+            auto stage = [&](const uint32_t (&q)[16], const uint32_t (&q2)[16]) {
                 if (lane == 0) bulk_wait_read();
                 __syncwarp();
                 // 16-byte chunk j of row `lane` goes to chunk j ^ (lane % 8) (128-byte swizzle)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(q0[4 * j], q0[4 * j + 1], q0[4 * j + 2], q0[4 * j + 3]);
+                        make_uint4(q[4 * j], q[4 * j + 1], q[4 * j + 2], q[4 * j + 3]);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     *reinterpret_cast<uint4*>(my_row + (((j + 4) ^ (lane & 7)) << 4)) =
-                        make_uint4(q1[4 * j], q1[4 * j + 1], q1[4 * j + 2], q1[4 * j + 3]);
+                        make_uint4(q2[4 * j], q2[4 * j + 1], q2[4 * j + 2], q2[4 * j + 3]);
+            };
+            auto store = [&](int64_t x) {
                 fence_proxy_async_smem();
                 __syncwarp();
-                const int64_t x = n_half + rnd * 64;
                 if (lane == 0 && row0 < p.M && x < p.N) {
                     tma_store_2d(&tma_y, box, static_cast<int32_t>(x), static_cast<int32_t>(row0));
                     bulk_commit();
                 }
+            };
+            // Round 0 is scaled and staged before round 1 is loaded, so the
+            // accumulator is released after two TMEM round trips and one round
+            // of arithmetic; the rest of the tile's output work follows.
+            {
+                uint32_t r0[32], r1[32], qa[16], qb[16];
+                tmem_ld32(t_base, r0);
+                tmem_ld32(t_base + 32, r1);
+                tmem_wait(r0);
+                reg_fence(r1);
+                scale_chunk(r0, sb_s, sa, qa);
+                scale_chunk(r1, sb_s + 32, sa, qb);
+                stage(qa, qb);
+            }
+            {
+                uint32_t r0[32], r1[32], qa[16], qb[16];
+                tmem_ld32(t_base + 64, r0);
+                tmem_ld32(t_base + 96, r1);
+                tmem_wait(r0);
+                reg_fence(r1);
+                // every accumulator read of this tile is complete
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+                store(n_half);
+                scale_chunk(r0, sb_s + 64, sa, qa);
+                scale_chunk(r1, sb_s + 96, sa, qb);
+                stage(qa, qb);
+                store(n_half + 64);
             }
             acc_phase ^= 1u;
         }
@@ -1057,7 +1084,7 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
     if (resident[ctx.device & 63] == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(ctx.sm_count & ~1), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(kPThreads, 1, 1);
         cfg.dynamicSmemBytes = kPSmemBytes;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
@@ -1069,7 +1096,7 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
     const int64_t cap = resident[ctx.device & 63];
     const int64_t pairs = pair_tiles < cap ? pair_tiles : cap;
     if (pairs <= 0) return NVFP4_OK;
-    nvfp4_gemm_pair_kernel<<<static_cast<int>(2 * pairs), kThreads, kPSmemBytes, s>>>(ma, mb, my, p);
+    nvfp4_gemm_pair_kernel<<<static_cast<int>(2 * pairs), kPThreads, kPSmemBytes, s>>>(ma, mb, my, p);
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;
 }
