@@ -10,30 +10,37 @@
 // path slower than BF16; "TRIAGE", section "NVFP4 quantization format and W4A4
 // execution": W4A4 runs natively on the tensor cores).
 //
-// One persistent CTA per SM, warp-specialised:
-//   warp 0      TMA producer: A/B tiles (cp.async.bulk.tensor, 128B swizzle) and
-//               the swizzled scale tiles (cp.async.bulk) into a 4-stage ring.
-//   warp 1      TMEM allocator + MMA issuer: tcgen05.mma accumulates the 128 x 256
-//               output tile in TMEM, tcgen05.commit releases ring stages.
+// Both GEMMs run on two-SM clusters (tcgen05 cta_group::2): the even CTA of a
+// pair issues M = 256, N = 256 MMAs whose A rows come from both CTAs' shared
+// memory (128 each) and whose 256 B rows are split 128/128 between them; each
+// CTA holds its own 128 x 256 FP32 accumulator in TMEM.  Persistent: one pair
+// per two SMs, tiles strided over the pairs.  Per CTA, warp-specialised:
+//   warp 0 / warp 14  TMA producers (A and its scales / this CTA's B rows and
+//               the B scales) into a 5-stage shared-memory ring; two issuing
+//               threads because one thread's TMA copies are processed serially.
+//   warp 1      TMEM allocation (collective across the pair); in the even CTA
+//               the MMA issuer: warp-uniform loop, one elected lane issues the
+//               MMAs and the multicast commits that release both CTAs' stages.
 //   warps 2..5  scale warps, one per TMEM lane quadrant: each reads the stage's
 //               512-byte scale atoms from shared memory (line = lane) and writes
 //               them into its own 32 TMEM lanes with tcgen05.st -- the same
 //               4-way replicated image a tcgen05.cp 32x128b.warpx4 would make,
 //               but on the warps' TMEM store path, which (measured) overlaps the
-//               MMAs, whereas every tcgen05.cp occupies the serial MMA pipe.
+//               MMAs, whereas every tcgen05.cp occupies the serial MMA pipe --
+//               then arrive on the even CTA's barrier.
 //   warps 6..13 epilogue, two warps per TMEM lane quadrant (128 columns each):
-//               stage S_b in shared memory and load S_a while the tile is still
-//               accumulating, then tcgen05.ld the accumulator 32 columns at a
-//               time (the second warp of the quadrant overlaps the first), scale
-//               by S_a * S_b with packed FP32x2 multiplies, round to bf16,
-//               release the accumulator, store.
-// Tile 128 x 256 x 256 (K step of 256 FP4 = 128 bytes = one swizzle row).
-// The grouped (MoE) variant walks the padded per-expert layout: each 128-row
-// tile belongs to one expert, found from the device-side offsets.
+//               tcgen05.ld 64 columns at a time, scale by S_a * S_b with packed
+//               FP32x2 multiplies, round to bf16, stage in 128-byte swizzled
+//               shared memory and store with TMA; the accumulator is released
+//               after the second load, before any store.
+// Tile 256 x 256 per pair, K step of 256 FP4 = 128 bytes = one swizzle row.
+// The grouped (MoE) variant walks the padded per-expert layout (128-row
+// aligned segments, device-side offsets): a pair tile covers two 128-row tiles
+// of one expert.
 //
 // Every wait is bounded: a wait that runs out sets the status word and a shared
-// abort flag, every role leaves its loop, the producer waits (bounded) for its
-// copies in flight, the MMA thread for its tensor-core work, and TMEM is freed.
+// abort flag, every role leaves its loop, the producers wait (bounded) for their
+// copies in flight, the MMA warp for its tensor-core work, and TMEM is freed.
 // (The scale warps' tcgen05.st are complete before they signal, so they leave
 // nothing in flight.)
 #include <cuda.h>
@@ -46,15 +53,12 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBKBytes = 128;                // 256 FP4 values per K step
-constexpr int kStages = 4;
 constexpr int kMmaPerStage = 4;              // K = 64 per tcgen05.mma
 constexpr int kSFWarps = 4;                  // one per TMEM lane quadrant
 constexpr int kEpiWarps = 8;                 // two per TMEM lane quadrant, 128 columns each
 constexpr int kFirstSFWarp = 2;
 constexpr int kFirstEpiWarp = kFirstSFWarp + kSFWarps;
-constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr uint32_t kATileBytes = kBM * kBKBytes;      // 16 KB
-constexpr uint32_t kBTileBytes = kBN * kBKBytes;      // 32 KB
 constexpr uint32_t kSFAtomBytes = 512;                // 128 rows x 4 scales
 constexpr uint32_t kSFATileBytes = 4 * kSFAtomBytes;  // 2 KB per stage
 constexpr uint32_t kSFBTileBytes = 8 * kSFAtomBytes;  // 4 KB per stage
@@ -62,15 +66,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSFTmemCol = 256;                  // after the 256 accumulator columns
 constexpr uint32_t kSFTmemPerStage = 48;              // 16 (A) + 32 (B)
 constexpr uint32_t kSBBytes = kEpiWarps * (kBN / 2) * 4; // per-warp copy of the tile's S_b half
-constexpr size_t kSmemBytes =
-    1024 + kStages * (kATileBytes + kBTileBytes + kSFATileBytes + kSFBTileBytes) + kSBBytes + 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;      // 0.2 s
-
-// Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), K-major,
-// N = 256 (N >> 3 at bit 17), M = 128 (M >> 4 at bit 24), scales UE4M3 (bit 23
-// clear), scale-factor ids 0, dense.
-constexpr uint32_t kInstrDesc = (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) | ((kBM >> 4) << 24);
 
 struct GemmParams {
     const uint8_t* sfa;
@@ -118,29 +115,12 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(smem_u32(bar)) : "memory");
-}
-
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (SBO), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(const void* p) {
     const uint64_t addr = smem_u32(p);
     return ((addr >> 4) & 0x3FFFull) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) |
            (2ull << 61);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate, uint32_t sfa_tmem, uint32_t sfb_tmem) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kInstrDesc), "r"(accumulate), "r"(sfa_tmem),
-          "r"(sfb_tmem)
-        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns; thread t gets lane (base + t).
@@ -248,327 +228,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ----------------------------------------------------------------------------
-// Tile schedule (identical in every role)
+// The pair kernel (tcgen05 cta_group::2)
 // ----------------------------------------------------------------------------
-struct Tile {
-    int64_t m0;        // first row of A / Y
-    int64_t n0;        // first column of Y (row of B inside the expert)
-    int64_t b_row0;    // first row of B in the stacked [E * N] weights
-    int m_tile;        // row tile of A's scales
-    int expert;
-};
-
-template <bool kGrouped>
-__device__ __forceinline__ int num_tiles(const GemmParams& p, int used_m_tiles) {
-    return (kGrouped ? used_m_tiles : p.num_m_tiles) * p.num_n_tiles;
-}
-
-template <bool kGrouped>
-__device__ __forceinline__ Tile tile_at(const GemmParams& p, int t, int used_m_tiles) {
-    Tile tl;
-    const int mt_count = kGrouped ? used_m_tiles : p.num_m_tiles;
-    tl.m_tile = t % mt_count;
-    const int nt = t / mt_count;
-    tl.m0 = static_cast<int64_t>(tl.m_tile) * kBM;
-    tl.n0 = static_cast<int64_t>(nt) * kBN;
-    tl.expert = 0;
-    if (kGrouped) {
-        // expert e with offsets[e] <= m0 < offsets[e + 1]
-        int lo = 0, hi = p.E - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (static_cast<int64_t>(__ldg(p.offsets + mid)) <= tl.m0) lo = mid;
-            else hi = mid - 1;
-        }
-        tl.expert = lo;
-    }
-    tl.b_row0 = static_cast<int64_t>(tl.expert) * p.N + tl.n0;
-    return tl;
-}
-
-template <bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                      const __grid_constant__ CUtensorMap tma_b, GemmParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = sA + kStages * kATileBytes;
-    uint8_t* sSFA = sB + kStages * kBTileBytes;
-    uint8_t* sSFB = sSFA + kStages * kSFATileBytes;
-    float* sSB = reinterpret_cast<float*>(sSFB + kStages * kSFBTileBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sSB) + kSBBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* sf_ready = empty + kStages;
-    uint64_t* acc_full = sf_ready + kStages;
-    uint64_t* acc_empty = acc_full + 1;
-    uint64_t* drain = acc_empty + 1;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    // Rows in use (grouped): the padded layout ends at offsets[E].
-    int used_m_tiles = p.num_m_tiles;
-    if (kGrouped) {
-        int64_t used = __ldg(p.offsets + p.E);
-        if (used > p.M || used < 0) {
-            if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
-            used = used < 0 ? 0 : p.M;
-        }
-        used_m_tiles = static_cast<int>((used + kBM - 1) / kBM);
-    }
-    const int tiles = num_tiles<kGrouped>(p, used_m_tiles);
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-            mbar_init(&sf_ready[s], kSFWarps);
-        }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kEpiWarps * 32);
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(tmem_holder)), "r"(kTmemCols) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_holder;
-
-    if (warp == 0 && lane == 0) {
-        // ------------------------------ producer ------------------------------
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_a)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_b)) : "memory");
-        uint32_t stage = 0, phase = 0;
-        uint32_t issued_mask = 0, last_phase = 0;
-        bool ok = true;
-        const int sfb_tiles_n = static_cast<int>((p.N + 127) / 128);
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            const Tile tl = tile_at<kGrouped>(p, t, used_m_tiles);
-            if (kGrouped && (__ldg(p.offsets + tl.expert) & (kBM - 1)) != 0)
-                record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
-            const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
-            const int nt128 = static_cast<int>(tl.n0 / 128);
-            const bool two_b_atoms = nt128 + 1 < sfb_tiles_n;
-            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
-                const uint32_t sf_bytes = ng * kSFAtomBytes;
-                const uint32_t bytes =
-                    kATileBytes + kBTileBytes + sf_bytes + (two_b_atoms ? 2 : 1) * sf_bytes;
-                mbar_arrive_expect_tx(&full[stage], bytes);
-                tma_load_2d(&tma_a, &full[stage], sA + stage * kATileBytes, kt * kBKBytes,
-                            static_cast<int32_t>(tl.m0));
-                tma_load_2d(&tma_b, &full[stage], sB + stage * kBTileBytes, kt * kBKBytes,
-                            static_cast<int32_t>(tl.b_row0));
-                const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
-                bulk_load(sSFA + stage * kSFATileBytes,
-                          p.sfa + (static_cast<int64_t>(tl.m_tile) * p.kgroups + g0) * kSFAtomBytes,
-                          sf_bytes, &full[stage]);
-                bulk_load(sSFB + stage * kSFBTileBytes,
-                          sfb_e + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes,
-                          sf_bytes, &full[stage]);
-                if (two_b_atoms)
-                    bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
-                              sfb_e + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
-                              sf_bytes, &full[stage]);
-                issued_mask |= 1u << stage;
-                last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
-        }
-        // every copy this thread issued must land before the CTA may exit
-        for (int s = 0; s < kStages; ++s)
-            if (issued_mask & (1u << s))
-                if (!mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kDrainLimitNs, nullptr))
-                    record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------ MMA issuer ----------------------------
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                // the scale warps have seen the stage full and put its scales in TMEM
-                if (!mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
-                const uint32_t sf_col = tmem + kSFTmemCol + stage * kSFTmemPerStage;
-                const uint8_t* a_s = sA + stage * kATileBytes;
-                const uint8_t* b_s = sB + stage * kBTileBytes;
-                for (int j = 0; j < ng; ++j) {
-                    tc_mma(tmem, sw128_desc(a_s + j * 32), sw128_desc(b_s + j * 32),
-                           (kt > 0 || j > 0) ? 1u : 0u, sf_col + j * 4, sf_col + 16 + j * 8);
-                }
-                tc_commit(&empty[stage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (!ok) break;
-            tc_commit(acc_full);
-            acc_phase ^= 1u;
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
-        }
-        // all tensor-core work issued by this thread completes before TMEM is freed
-        tc_commit(drain);
-        if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr))
-            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
-    } else if (warp >= kFirstSFWarp && warp < kFirstEpiWarp) {
-        // ------------------------------ scale warps ---------------------------
-        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-        uint32_t stage = 0, phase = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
-                got = __all_sync(0xFFFFFFFFu, got);
-                if (!got) {
-                    ok = false;
-                    break;
-                }
-                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
-                // line `lane` of every 512-byte atom = 16 bytes = 4 TMEM columns
-                const uint4* sfa_s = reinterpret_cast<const uint4*>(sSFA + stage * kSFATileBytes);
-                const uint4* sfb_s = reinterpret_cast<const uint4*>(sSFB + stage * kSFBTileBytes);
-                uint32_t va[16], vb[32];
-#pragma unroll
-                for (int j = 0; j < kMmaPerStage; ++j) {
-                    const uint4 a = (j < ng) ? sfa_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 b0 = (j < ng) ? sfb_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 b1 = (j < ng) ? sfb_s[(kSFATileBytes / 16) + j * 32 + lane]
-                                              : make_uint4(0u, 0u, 0u, 0u);
-                    va[4 * j] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
-                    vb[8 * j] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
-                    vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z;
-                    vb[8 * j + 7] = b1.w;
-                }
-                const uint32_t sf_col = tmem + t_lane + kSFTmemCol + stage * kSFTmemPerStage;
-                tmem_st16(sf_col, va);
-                tmem_st32(sf_col + 16, vb);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sf_ready[stage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
-        }
-    } else if (warp >= kFirstEpiWarp) {
-        // ------------------------------ epilogue ------------------------------
-        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const int half = (warp - kFirstEpiWarp) >> 2;   // which 128 columns of the tile
-        const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
-        float* sb_s = sSB + (warp - kFirstEpiWarp) * (kBN / 2);
-        uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-            // scales first: their loads overlap the tile's main loop
-            const Tile tl = tile_at<kGrouped>(p, t, used_m_tiles);
-            const int64_t m = tl.m0 + quad * 32 + lane;
-            const float sa = (m < p.M) ? __ldg(p.sa + m) : 0.0f;
-            const int64_t n_half = tl.n0 + half * (kBN / 2);
-            const float* sbp = p.sb + (kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half;
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < kBN / 2 / 32; ++i) {
-                const int64_t n = n_half + i * 32 + lane;
-                sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + i * 32 + lane) : 0.0f;
-            }
-            __syncwarp();
-            bool ok = mbar_wait_bounded(acc_full, acc_phase, kWaitLimitNs, abort_flag);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) {
-                *abort_flag = 1;
-                if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_EPILOGUE);
-                break;
-            }
-            tc_fence_after();
-            uint32_t packed[kBN / 4];
-#pragma unroll
-            for (int c = 0; c < kBN / 64; ++c) {
-                uint32_t r[32];
-                tmem_ld32(t_base + c * 32, r);
-                tmem_wait(r);
-                scale_chunk(r, sb_s + c * 32, sa, packed + c * 16);
-            }
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-            acc_phase ^= 1u;
-            if (m < p.M) {
-                uint16_t* yrow = p.y + m * p.ld_y + n_half;
-#pragma unroll
-                for (int v = 0; v < kBN / 2 / 8; ++v) {
-                    if (n_half + v * 8 < p.N)
-                        reinterpret_cast<uint4*>(yrow)[v] =
-                            make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                       packed[4 * v + 3]);
-                }
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmemCols) : "memory");
-    }
-}
-
-// ----------------------------------------------------------------------------
-// Dense GEMM on CTA pairs (tcgen05 cta_group::2)
-// ----------------------------------------------------------------------------
-// A cluster of two CTAs on two SMs computes one 256 x 256 output tile with
-// M = 256 MMAs issued by the even CTA: each CTA stages its own 128 rows of A and
-// one 128-row half of the B tile, so per SM each 256-deep K step moves 32 KB of
-// operands into shared memory instead of 48 KB, and the tensor core reads the
-// peer's B half from the peer SM.  Each CTA keeps its 128 x 256 FP32 accumulator
-// and the scale factors of its own MMA rows (A) and of all 256 B rows in its own
-// TMEM, written by its own scale warps.  Cross-CTA signals:
+// Each CTA stages its own 128 rows of A and one 128-row half of the B tile, so
+// per SM each 256-deep K step moves 32 KB of operands into shared memory
+// instead of the 48 KB a single-SM 128 x 256 tile needs.  Each CTA keeps its
+// accumulator and the scale factors of its own MMA rows (A) and of all 256 B
+// rows in its own TMEM, written by its own scale warps.  Cross-CTA signals:
 //   scale warps (both CTAs) -> sf_ready of the even CTA (remote mbarrier arrive),
 //   MMA commits            -> empty / acc_full of both CTAs (multicast commit),
 //   epilogue (both CTAs)   -> acc_empty of the even CTA (remote arrive).
 constexpr int kPStages = 5;
 constexpr int kPBWarp = kFirstEpiWarp + kEpiWarps;                // the B-side producer
 constexpr int kPThreads = 32 * (kPBWarp + 1);
+constexpr int kPLoadLanes = 1;                                    // issuing lanes per producer warp
+constexpr unsigned kPLoadMask = (1u << kPLoadLanes) - 1;
+constexpr int kPBoxRows = 128 / kPLoadLanes;                      // rows of A or B per TMA box
 constexpr uint32_t kPBHalfBytes = 128 * kBKBytes;                 // 16 KB
 // Output staging: per epilogue warp one 32-row x 64-column bf16 box (4 KB),
 // 128-byte swizzled so the tensor-map store reads it back in rows.
@@ -578,7 +253,9 @@ constexpr uint32_t kPCarveBytes = kPStages * (kATileBytes + kPBHalfBytes + kSFAT
                                   kPOutBytes + kSBBytes + 256;
 constexpr size_t kPSmemBytes = 232448;                            // the opt-in maximum (227 KB)
 static_assert(kPCarveBytes + 512 <= kPSmemBytes, "shared memory carve-up");
-// M = 256 across the pair (M >> 4 at bit 24), N = 256.
+// Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1 at bits 7 and
+// 10), K-major, N = 256 (N >> 3 at bit 17), M = 256 across the pair (M >> 4 at
+// bit 24), scales UE4M3 (bit 23 clear), scale-factor ids 0, dense.
 constexpr uint32_t kPInstrDesc = (1u << 7) | (1u << 10) | ((256u >> 3) << 17) | ((256u >> 4) << 24);
 static_assert(kSFTmemCol + kPStages * kSFTmemPerStage <= kTmemCols, "TMEM columns");
 
@@ -665,6 +342,55 @@ __device__ __forceinline__ void cluster_sync_all() {
                  ::: "memory");
 }
 
+// One 256 x 256 output tile of a CTA pair.
+struct PairTile {
+    bool run;          // grouped: false for a slot that does not start a pair tile
+    int64_t m_base;    // first row of the pair; CTA r owns rows m_base + 128 r ..
+    int64_t n0;        // first output column
+    int64_t b_row0;    // first row of B in the (stacked) weights
+    int64_t row_end;   // rows at or past this are not written: M, or the expert's end
+    int expert;
+};
+
+// Dense: t -> (m-tile, n-tile), m fastest.  Grouped: t -> (128-row tile g of
+// the padded layout, n-tile), n fastest; a pair tile starts at every second
+// 128-row tile of an expert's segment, so an expert with an odd number of
+// tiles ends in a tile whose odd CTA reads rows past the expert (its results
+// are computed with this expert's B and never stored).
+template <bool kGrouped>
+__device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int num_pm) {
+    PairTile tl;
+    if (!kGrouped) {
+        const int mt = t % num_pm;
+        const int nt = t / num_pm;
+        tl.run = true;
+        tl.m_base = static_cast<int64_t>(mt) * 256;
+        tl.n0 = static_cast<int64_t>(nt) * kBN;
+        tl.b_row0 = tl.n0;
+        tl.row_end = p.M;
+        tl.expert = 0;
+        return tl;
+    }
+    const int nt = t % p.num_n_tiles;
+    const int64_t m0 = static_cast<int64_t>(t / p.num_n_tiles) * 128;
+    // the last expert e with offsets[e] <= m0 (empty experts are passed over)
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(__ldg(p.offsets + mid)) <= m0) lo = mid;
+        else hi = mid - 1;
+    }
+    const int64_t e_begin = __ldg(p.offsets + lo);
+    tl.run = (((m0 - e_begin) >> 7) & 1) == 0;
+    tl.m_base = m0;
+    tl.n0 = static_cast<int64_t>(nt) * kBN;
+    tl.b_row0 = static_cast<int64_t>(lo) * p.N + tl.n0;
+    tl.row_end = __ldg(p.offsets + lo + 1);
+    tl.expert = lo;
+    return tl;
+}
+
+template <bool kGrouped>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                            const __grid_constant__ CUtensorMap tma_b,
@@ -699,7 +425,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int pair = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
     const int num_pm = static_cast<int>((p.M + 255) / 256);
-    const int tiles = num_pm * p.num_n_tiles;
+    int tiles = num_pm * p.num_n_tiles;
+    if (kGrouped) {
+        // slots of the padded layout in use: it ends at offsets[E]
+        int64_t used = __ldg(p.offsets + p.E);
+        if (used > p.M || used < 0) {
+            if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
+            used = used < 0 ? 0 : p.M;
+        }
+        tiles = static_cast<int>((used + 127) / 128) * p.num_n_tiles;
+    }
     const int a_row_tiles = static_cast<int>((p.M + 127) / 128);
     const int sfb_tiles_n = static_cast<int>((p.N + 127) / 128);
 
@@ -727,54 +462,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if ((warp == 0 || warp == kPBWarp) && lane == 0) {
+    if ((warp == 0 || warp == kPBWarp) && lane < kPLoadLanes) {
         // ------------------------------ producers (both CTAs) ------------------
-        // Two threads in two warps feed each stage: warp 0 loads A and its
-        // scales, warp kPBWarp this CTA's half of B and the B scales.  (TMA
-        // copies issued by one thread complete one after another; two issuing
-        // threads double the rate at which a stage fills.)
+        // Warp 0 loads A and its scales, warp kPBWarp this CTA's 128 rows of B
+        // and the B scales; kPLoadLanes lanes of each split the rows.  TMA
+        // copies issued by one thread are processed one after another (about
+        // 27 bytes per SM clock for 16 KB tiles), so a stage fills at the rate
+        // of its issuing threads.  (Two warps with one lane each measured
+        // fastest: 64-row boxes from two lanes each were slower.)
         const bool side_b = warp == kPBWarp;
+        const int sub = lane;                     // which kPBoxRows-row part
         const CUtensorMap* map = side_b ? &tma_b : &tma_a;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
         uint32_t stage = 0, phase = 0;
         uint32_t issued_mask = 0, last_phase = 0;
         bool ok = true;
         for (int t = pair; t < tiles && ok; t += npairs) {
-            const int mt = t % num_pm;
-            const int nt = t / num_pm;
-            const int64_t m0 = static_cast<int64_t>(mt) * 256 + rank * 128;
-            const int64_t n0 = static_cast<int64_t>(nt) * kBN;
+            const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
+            if (!tl.run) continue;
+            if (kGrouped && !side_b && rank == 0 && (__ldg(p.offsets + tl.expert) & 127) != 0)
+                record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
+            const int64_t m0 = tl.m_base + rank * 128;
+            const int64_t n0 = tl.n0;
             const int a_tile = static_cast<int>(m0 / 128);
             const bool a_sf_ok = a_tile < a_row_tiles;
             const int nt128 = static_cast<int>(n0 / 128);
             const bool two_b_atoms = nt128 + 1 < sfb_tiles_n;
+            const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
             for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(kPLoadMask,
+                                mbar_wait_cluster(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag));
+                if (!ok) break;
                 const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
                 const uint32_t sf_bytes = ng * kSFAtomBytes;
                 const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
+                // lane 0 announces the side's bytes before any of its copies is issued
+                if (sub == 0)
+                    mbar_arrive_expect_tx(&full[stage], side_b ? kPBHalfBytes + (two_b_atoms ? 2u : 1u) * sf_bytes
+                                                               : kATileBytes + (a_sf_ok ? sf_bytes : 0u));
+                __syncwarp(kPLoadMask);
                 if (!side_b) {
-                    mbar_arrive_expect_tx(&full[stage], kATileBytes + (a_sf_ok ? sf_bytes : 0u));
-                    tma_load_2d(map, &full[stage], sA + stage * kATileBytes, kt * kBKBytes,
-                                static_cast<int32_t>(m0));
-                    if (a_sf_ok)
+                    tma_load_2d(map, &full[stage], sA + stage * kATileBytes + sub * kPBoxRows * kBKBytes,
+                                kt * kBKBytes, static_cast<int32_t>(m0 + kPBoxRows * sub));
+                    if (a_sf_ok && sub == 0)
                         bulk_load(sSFA + stage * kSFATileBytes,
                                   p.sfa + (static_cast<int64_t>(a_tile) * p.kgroups + g0) * kSFAtomBytes,
                                   sf_bytes, &full[stage]);
                 } else {
-                    mbar_arrive_expect_tx(&full[stage], kPBHalfBytes + (two_b_atoms ? 2u : 1u) * sf_bytes);
-                    tma_load_2d(map, &full[stage], sB + stage * kPBHalfBytes, kt * kBKBytes,
-                                static_cast<int32_t>(n0 + rank * 128));
-                    bulk_load(sSFB + stage * kSFBTileBytes,
-                              p.sfb + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
-                              &full[stage]);
-                    if (two_b_atoms)
-                        bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
-                                  p.sfb + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
-                                  sf_bytes, &full[stage]);
+                    tma_load_2d(map, &full[stage], sB + stage * kPBHalfBytes + sub * kPBoxRows * kBKBytes,
+                                kt * kBKBytes, static_cast<int32_t>(tl.b_row0 + rank * 128 + kPBoxRows * sub));
+                    if (sub == 0) {
+                        bulk_load(sSFB + stage * kSFBTileBytes,
+                                  sfb_e + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
+                                  &full[stage]);
+                        if (two_b_atoms)
+                            bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
+                                      sfb_e + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
+                                      sf_bytes, &full[stage]);
+                    }
                 }
                 issued_mask |= 1u << stage;
                 last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -786,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
         if (!ok) {
             *abort_flag = 1;
-            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
+            if (sub == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
         }
         // every copy this thread issued must land before the CTA may exit
         for (int s = 0; s < kPStages; ++s)
@@ -802,6 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         const uint64_t a_desc0 = sw128_desc(sA);
         const uint64_t b_desc0 = sw128_desc(sB);
         for (int t = pair; t < tiles && ok; t += npairs) {
+            if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
             ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -856,6 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         for (int t = pair; t < tiles && ok; t += npairs) {
+            if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
             for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                 bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
                 got = __all_sync(0xFFFFFFFFu, got);
@@ -912,13 +659,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         const uint32_t acc_empty_leader = peer_addr(acc_empty, 0);
         uint32_t acc_phase = 0;
         for (int t = pair; t < tiles; t += npairs) {
-            const int mt = t % num_pm;
-            const int nt = t / num_pm;
-            const int64_t row0 = static_cast<int64_t>(mt) * 256 + rank * 128 + quad * 32;
+            const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
+            if (!tl.run) continue;
+            // this CTA's 128 rows lie inside the tile's row range, or wholly past it
+            const bool write = tl.m_base + rank * 128 < tl.row_end;
+            const int64_t row0 = tl.m_base + rank * 128 + quad * 32;
             const int64_t m = row0 + lane;
             const float sa = (m < p.M) ? __ldg(p.sa + m) : 0.0f;
-            const int64_t n_half = static_cast<int64_t>(nt) * kBN + half * (kBN / 2);
-            const float* sbp = p.sb + n_half;
+            const int64_t n_half = tl.n0 + half * (kBN / 2);
+            const float* sbp = p.sb + (kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half;
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < kBN / 2 / 32; ++i) {
@@ -953,7 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             auto store = [&](int64_t x) {
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && row0 < p.M && x < p.N) {
+                if (lane == 0 && write && row0 < p.M && x < p.N) {
                     tma_store_2d(&tma_y, box, static_cast<int32_t>(x), static_cast<int32_t>(row0));
                     bulk_commit();
                 }
@@ -1052,28 +801,11 @@ bool make_map_y(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_
 }
 
 template <bool kGrouped>
-nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
-                         int tiles_upper, const DeviceCtx& ctx, cudaStream_t s) {
-    static bool attr_set[64] = {};
-    if (!attr_set[ctx.device & 63]) {
-        if (cudaFuncSetAttribute(nvfp4_gemm_kernel<kGrouped>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
-            return NVFP4_ERR_CUDA;
-        attr_set[ctx.device & 63] = true;
-    }
-    const int grid = tiles_upper < ctx.sm_count ? tiles_upper : ctx.sm_count;
-    if (grid <= 0) return NVFP4_OK;
-    nvfp4_gemm_kernel<kGrouped><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, p);
-    NVFP4_CHECK_LAUNCH();
-    return NVFP4_OK;
-}
-
 nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
                               const GemmParams& p, int64_t pair_tiles, const DeviceCtx& ctx, cudaStream_t s) {
     static bool attr_set[64] = {};
     if (!attr_set[ctx.device & 63]) {
-        if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kPSmemBytes)) != cudaSuccess)
             return NVFP4_ERR_CUDA;
         attr_set[ctx.device & 63] = true;
@@ -1087,7 +819,7 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
         cfg.blockDim = dim3(kPThreads, 1, 1);
         cfg.dynamicSmemBytes = kPSmemBytes;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel<kGrouped>, &cfg) != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
             n = ctx.sm_count / 2;
         }
@@ -1096,7 +828,7 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
     const int64_t cap = resident[ctx.device & 63];
     const int64_t pairs = pair_tiles < cap ? pair_tiles : cap;
     if (pairs <= 0) return NVFP4_OK;
-    nvfp4_gemm_pair_kernel<<<static_cast<int>(2 * pairs), kPThreads, kPSmemBytes, s>>>(ma, mb, my, p);
+    nvfp4_gemm_pair_kernel<kGrouped><<<static_cast<int>(2 * pairs), kPThreads, kPSmemBytes, s>>>(ma, mb, my, p);
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;
 }
@@ -1130,7 +862,7 @@ nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int
         return NVFP4_ERR_ALIGNMENT;
     CUtensorMap ma, mb, my;
     // pairs of CTAs: each loads a 128-row half of the 256-row B tile
-    if (!make_map(&ma, a_q, M, K / 2, kBM) || !make_map(&mb, b_q, N, K / 2, 128) ||
+    if (!make_map(&ma, a_q, M, K / 2, kPBoxRows) || !make_map(&mb, b_q, N, K / 2, kPBoxRows) ||
         !make_map_y(&my, y, M, N, ld_y))
         return NVFP4_ERR_CUDA;
     GemmParams p;
@@ -1152,7 +884,7 @@ nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int
     p.E = 0;
     const int64_t pair_tiles = ceil_div(M, 256) * p.num_n_tiles;
     if (pair_tiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
-    return launch_gemm_pair(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_pair<false>(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* a_s,
@@ -1171,9 +903,10 @@ nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* 
     if (!aligned(a_q, 16) || !aligned(b_q, 16) || !aligned(a_sf, 16) || !aligned(b_sf, 16) ||
         !aligned(y, 16) || !aligned(a_s, 4) || !aligned(b_s, 4) || !aligned(expert_offsets, 4))
         return NVFP4_ERR_ALIGNMENT;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, a_q, rows_capacity, K / 2, kBM) ||
-        !make_map(&mb, b_q, static_cast<int64_t>(E) * N, K / 2, kBN))
+    CUtensorMap ma, mb, my;
+    if (!make_map(&ma, a_q, rows_capacity, K / 2, kPBoxRows) ||
+        !make_map(&mb, b_q, static_cast<int64_t>(E) * N, K / 2, kPBoxRows) ||
+        !make_map_y(&my, y, rows_capacity, N, N))
         return NVFP4_ERR_CUDA;
     GemmParams p;
     p.sfa = static_cast<const uint8_t*>(a_sf);
@@ -1192,10 +925,10 @@ nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* 
     p.num_n_tiles = static_cast<int>(ceil_div(N, kBN));
     p.num_m_tiles = static_cast<int>(ceil_div(rows_capacity, kBM));
     p.E = E;
-    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
-    if (tiles > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
-    return launch_gemm<true>(ma, mb, p, static_cast<int>(tiles), ctx,
-                             reinterpret_cast<cudaStream_t>(stream));
+    // slots: every 128-row tile of the capacity x every n-tile (about half start a pair tile)
+    const int64_t slots = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+    if (slots > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
+    return launch_gemm_pair<true>(ma, mb, my, p, (slots + 1) / 2, ctx, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
