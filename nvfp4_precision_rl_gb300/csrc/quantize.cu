@@ -254,6 +254,36 @@ struct ColParams {
 
 constexpr int kColThreads = 128;
 
+// |a| max |b| on bf16 pairs (exact: max of bf16 values).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t v) {
+    uint32_t out;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(m), "r"(v & 0x7FFF7FFFu));
+    return out;
+}
+
+// Codes of one column's 16-token block: tokens t (low nibble) and t + 1 (high).
+// `sel` picks the column's half of each 32-bit pair of columns.
+template <bool kHi>
+__device__ __forceinline__ uint2 encode_col_block(const uint32_t* v, float r) {
+    const float2 rr = make_float2(r, r);
+    uint32_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float x0 = kHi ? bf16hi(v[2 * i]) : bf16lo(v[2 * i]);
+        const float x1 = kHi ? bf16hi(v[2 * i + 1]) : bf16lo(v[2 * i + 1]);
+        const float2 y = __fmul2_rn(make_float2(x0, x1), rr);
+        b[i] = cvt_e2m1x2(y.x, y.y);
+    }
+    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                      b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+// Column-wise copy: thread = 2 adjacent columns (one 32-bit load per token) x
+// 64 tokens (4 blocks of 16 = one swizzled scale word per column); all 64 loads
+// are in flight before any arithmetic.  Amax uses packed bf16 max, the
+// multiply packed FP32x2; each column's 32 code bytes of the group are written
+// as two 16-byte stores when the row pitch allows it.
+template <bool kGather>
 __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -266,55 +296,57 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.s[0] = rec.S;
 
     uint32_t v[64];
+    if (!kGather && col_ok && m0 + 64 <= p.rows_out) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.x + m0 * p.ld_x + k0);
+        const int64_t step = p.ld_x >> 1;   // 32-bit words per row
 #pragma unroll
-    for (int t = 0; t < 64; ++t) {
-        const int64_t m = m0 + t;
-        int64_t src = -1;
-        if (m < p.rows_out) {
-            src = p.gather ? static_cast<int64_t>(p.gather[m]) : m;
-            if (src >= p.rows_in) src = -1;   // reported by the row pass
+        for (int t = 0; t < 64; ++t) v[t] = __ldg(src + t * step);
+    } else {
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+            const int64_t m = m0 + t;
+            int64_t src = -1;
+            if (m < p.rows_out) {
+                src = kGather ? static_cast<int64_t>(p.gather[m]) : m;
+                if (src >= p.rows_in) src = -1;   // reported by the row pass
+            }
+            v[t] = (col_ok && src >= 0)
+                       ? __ldg(reinterpret_cast<const uint32_t*>(p.x + src * p.ld_x + k0))
+                       : 0u;
         }
-        v[t] = (col_ok && src >= 0)
-                   ? __ldg(reinterpret_cast<const uint32_t*>(p.x + src * p.ld_x + k0))
-                   : 0u;
     }
     uint32_t word0 = 0u, word1 = 0u;
-    const int64_t qstride = p.rows_out >> 1;
+    uint2 c0[4], c1[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        float a0 = 0.0f, a1 = 0.0f;
+        uint32_t m = 0u;
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            a0 = fmaxf(a0, fabsf(bf16lo(v[16 * b + t])));
-            a1 = fmaxf(a1, fabsf(bf16hi(v[16 * b + t])));
-        }
+        for (int t = 0; t < 16; ++t) m = bf16x2_absmax(m, v[16 * b + t]);
         float r0, r1;
-        const uint32_t s0 = rec.block(a0, &r0);
-        const uint32_t s1 = rec.block(a1, &r1);
+        const uint32_t s0 = rec.block(bf16lo(m), &r0);
+        const uint32_t s1 = rec.block(bf16hi(m), &r1);
         word0 |= s0 << (8 * b);
         word1 |= s1 << (8 * b);
-        const uint32_t* vb = v + 16 * b;
-        uint2 c0, c1;
-        c0.x = cvt_e2m1x8(__fmul_rn(bf16lo(vb[0]), r0), __fmul_rn(bf16lo(vb[1]), r0),
-                          __fmul_rn(bf16lo(vb[2]), r0), __fmul_rn(bf16lo(vb[3]), r0),
-                          __fmul_rn(bf16lo(vb[4]), r0), __fmul_rn(bf16lo(vb[5]), r0),
-                          __fmul_rn(bf16lo(vb[6]), r0), __fmul_rn(bf16lo(vb[7]), r0));
-        c0.y = cvt_e2m1x8(__fmul_rn(bf16lo(vb[8]), r0), __fmul_rn(bf16lo(vb[9]), r0),
-                          __fmul_rn(bf16lo(vb[10]), r0), __fmul_rn(bf16lo(vb[11]), r0),
-                          __fmul_rn(bf16lo(vb[12]), r0), __fmul_rn(bf16lo(vb[13]), r0),
-                          __fmul_rn(bf16lo(vb[14]), r0), __fmul_rn(bf16lo(vb[15]), r0));
-        c1.x = cvt_e2m1x8(__fmul_rn(bf16hi(vb[0]), r1), __fmul_rn(bf16hi(vb[1]), r1),
-                          __fmul_rn(bf16hi(vb[2]), r1), __fmul_rn(bf16hi(vb[3]), r1),
-                          __fmul_rn(bf16hi(vb[4]), r1), __fmul_rn(bf16hi(vb[5]), r1),
-                          __fmul_rn(bf16hi(vb[6]), r1), __fmul_rn(bf16hi(vb[7]), r1));
-        c1.y = cvt_e2m1x8(__fmul_rn(bf16hi(vb[8]), r1), __fmul_rn(bf16hi(vb[9]), r1),
-                          __fmul_rn(bf16hi(vb[10]), r1), __fmul_rn(bf16hi(vb[11]), r1),
-                          __fmul_rn(bf16hi(vb[12]), r1), __fmul_rn(bf16hi(vb[13]), r1),
-                          __fmul_rn(bf16hi(vb[14]), r1), __fmul_rn(bf16hi(vb[15]), r1));
-        const int64_t mb = m0 + 16 * b;
-        if (col_ok && mb < p.rows_out) {
-            *reinterpret_cast<uint2*>(p.q + k0 * qstride + (mb >> 1)) = c0;
-            *reinterpret_cast<uint2*>(p.q + (k0 + 1) * qstride + (mb >> 1)) = c1;
+        c0[b] = encode_col_block<false>(v + 16 * b, r0);
+        c1[b] = encode_col_block<true>(v + 16 * b, r1);
+    }
+    if (col_ok) {
+        const int64_t qstride = p.rows_out >> 1;
+        uint8_t* q0 = p.q + k0 * qstride + (m0 >> 1);
+        uint8_t* q1 = q0 + qstride;
+        if (m0 + 64 <= p.rows_out && (qstride & 15) == 0) {
+            reinterpret_cast<uint4*>(q0)[0] = make_uint4(c0[0].x, c0[0].y, c0[1].x, c0[1].y);
+            reinterpret_cast<uint4*>(q0)[1] = make_uint4(c0[2].x, c0[2].y, c0[3].x, c0[3].y);
+            reinterpret_cast<uint4*>(q1)[0] = make_uint4(c1[0].x, c1[0].y, c1[1].x, c1[1].y);
+            reinterpret_cast<uint4*>(q1)[1] = make_uint4(c1[2].x, c1[2].y, c1[3].x, c1[3].y);
+        } else {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                if (m0 + 16 * b < p.rows_out) {
+                    reinterpret_cast<uint2*>(q0)[b] = c0[b];
+                    reinterpret_cast<uint2*>(q1)[b] = c1[b];
+                }
+            }
         }
     }
     // scale words (padding columns k >= cols get zero words)
@@ -434,7 +466,8 @@ nvfp4_status quantize_cols_launch(const uint16_t* x, int64_t rows_in, int64_t co
     }
     dim3 grid(static_cast<unsigned>(round_up(cols, 128) / 64),
               static_cast<unsigned>(ceil_div(p.kgroups, kColThreads / 32)));
-    quant_cols_kernel<<<grid, kColThreads, 0, stream>>>(p);
+    if (gather != nullptr) quant_cols_kernel<true><<<grid, kColThreads, 0, stream>>>(p);
+    else quant_cols_kernel<false><<<grid, kColThreads, 0, stream>>>(p);
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;
 }
