@@ -21,6 +21,8 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
                                  float64 matmul of the decoded operands)
   moe_permute                    pinned (numpy stable argsort, invariants)
   swiglu                         pinned (float64 closed form on exact inputs)
+  dequantize_bf16                pinned (hand-worked values, exact binary64
+                                 product within one bf16 rounding, round trip)
 """
 import ctypes
 import os
@@ -61,6 +63,7 @@ def lib():
         L.orc_moe_permute.restype = ctypes.c_int
         L.orc_swiglu.argtypes = [P, I64, I64, I64, P]
         L.orc_bf16_from_double.argtypes = [P, I64, P]
+        L.orc_dequantize_bf16.argtypes = [P, P, P, ctypes.c_int, I64, I64, P]
         _lib = L
     return _lib
 
@@ -170,6 +173,18 @@ def dequantize(q, sf_rm, s):
     cols = q.shape[1] * 2
     out = np.zeros((rows, cols), np.float64)
     lib().orc_dequantize(_p(q), _p(sf_rm), _p(s), rows, cols, _p(out))
+    return out
+
+
+def dequantize_bf16(q, sf_rm, s, s_per_row=True):
+    """bf16 bits of y = bf16_rn(fl32(S * dec(q) * dec(s_b))) (row-major scales)."""
+    q = _c(q, np.uint8)
+    sf_rm = _c(sf_rm, np.uint8)
+    s = _c(s, np.float32)
+    rows = q.shape[0]
+    cols = q.shape[1] * 2
+    out = np.zeros((rows, cols), np.uint16)
+    lib().orc_dequantize_bf16(_p(q), _p(sf_rm), _p(s), 1 if s_per_row else 0, rows, cols, _p(out))
     return out
 
 

@@ -335,6 +335,35 @@ ORC_API void orc_dequantize(const uint8_t* q, const uint8_t* sf_rm, const float*
         }
 }
 
+/* bf16 from binary32, round to nearest, ties to even (finite inputs; NaN kept). */
+static uint16_t bf16_from_float_rne(float f) {
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    if ((bits & 0x7F800000u) == 0x7F800000u && (bits & 0x007FFFFFu) != 0) return 0x7FC0;
+    uint32_t lower = bits & 0xFFFFu;
+    uint32_t upper = bits >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;   /* carries into the exponent */
+    return (uint16_t)upper;
+}
+
+/* Dequantization to bf16, the reading of the dequantized backward's input:
+ * c = dec(q) * dec(s_b) (exact in binary32), p = fl32(S * c), y = bf16_rn(p).
+ * s_per_row == 0: s[0] for every row. */
+ORC_API void orc_dequantize_bf16(const uint8_t* q, const uint8_t* sf_rm, const float* s, int s_per_row,
+                                 int64_t rows, int64_t cols, uint16_t* out) {
+    tables();
+    for (int64_t r = 0; r < rows; ++r) {
+        float S = s[s_per_row ? r : 0];
+        for (int64_t k = 0; k < cols; ++k) {
+            uint8_t byte = q[r * (cols / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            float c = (float)g_e2m1[code] * (float)g_e4m3[sf_rm[r * (cols / 16) + k / 16]];
+            float p = S * c;
+            out[r * cols + k] = bf16_from_float_rne(p);
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* W4A4 GEMM:  Y[m,n] = S_a[m] * S_b[n] * sum_k x^_mk w^_nk / (S_a S_b)       */
 /* ------------------------------------------------------------------------ */
