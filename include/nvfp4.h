@@ -270,6 +270,31 @@ NVFP4_API nvfp4_status nvfp4_grouped_gemm(
     void* y, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* Dequantize (NVFP4 -> BF16)                                                */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * y[r, k] = bf16_rn( fl32( S_r * fl32( dec(q[r, k]) * dec(s_b[r, k / 16]) ) ) ):
+ * the NVFP4 value x^ = S * dec(s_b) * dec(q) ("TRIAGE", section "NVFP4
+ * quantization format and W4A4 execution") evaluated in binary32 -- the
+ * code-times-block-scale product is exact, the multiply by the FP32 outer
+ * scale rounds once to binary32 -- then rounded to bf16, nearest-even.  Serves
+ * the dequantized-BF16 backward ("Towards Blackwell-Native 8-bit and 4-bit RL",
+ * NVFP4 backward modes).  Bit-exact.
+ *
+ *  q          packed E2M1 [rows, cols/2], low nibble = even k; 8-byte aligned.
+ *  sf         swizzled E4M3 block scales, nvfp4_sf_bytes(rows, cols) bytes.
+ *  s          float outer scales: s[r] when s_per_row != 0, else s[0] for every
+ *             row (the column-wise copy's single per-tensor scale).
+ *  cols       > 0, % 16 == 0.
+ *  y          bf16 [rows, ld_y], ld_y >= cols, ld_y % 8 == 0, 16-byte aligned.
+ *  Errors: NVFP4_ERR_SHAPE / _ALIGNMENT / _INVALID_ARG; rows == 0 is a no-op.
+ */
+NVFP4_API nvfp4_status nvfp4_dequantize(
+    const void* q, const void* sf, const float* s, int32_t s_per_row, int64_t rows, int64_t cols,
+    void* y, int64_t ld_y, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* SwiGLU + requantize (the MoE fc2 input)                                   */
 /* ------------------------------------------------------------------------- */
 

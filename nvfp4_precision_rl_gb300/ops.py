@@ -59,6 +59,7 @@ def lib():
         "nvfp4_gemm": (st, [P, P, P, I64, P, P, P, I64, I64, P, I64, P]),
         "nvfp4_grouped_gemm": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
         "nvfp4_swiglu_quantize": (st, [P, I64, I64, I64, P, P, P, P, P, P]),
+        "nvfp4_dequantize": (st, [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]),
         "nvfp4_get_device_status": (st, [P]),
         "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "nvfp4_debug_cvt_probe": (st, [P, P, P, P]),
@@ -147,6 +148,11 @@ def nvfp4_grouped_gemm(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_
     _ok("nvfp4_grouped_gemm", lib().nvfp4_grouped_gemm(
         _p(a_q), _p(a_sf), _p(a_s), rows_capacity, _p(expert_offsets), E, _p(b_q), _p(b_sf),
         _p(b_s), N, K, _p(y), _s(stream)))
+
+
+def nvfp4_dequantize(q, sf, s, s_per_row, rows, cols, y, ld_y, stream=None):
+    _ok("nvfp4_dequantize", lib().nvfp4_dequantize(
+        _p(q), _p(sf), _p(s), int(s_per_row), rows, cols, _p(y), ld_y, _s(stream)))
 
 
 def nvfp4_swiglu_quantize(y1, rows, ffn, ld_y1, row_count, q, sf, s, h=None, stream=None):
@@ -275,6 +281,20 @@ def grouped_gemm(a, expert_offsets, num_experts, b_q, b_sf, b_s, N, K, out=None,
     y = out if out is not None else torch.empty((rows, N), dtype=torch.bfloat16, device=a["q"].device)
     nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], rows, expert_offsets, num_experts, b_q, b_sf, b_s,
                        N, K, y, stream)
+    return y
+
+
+def dequantize(qres, column=False, out=None, stream=None):
+    """bf16 values of a quantize() result: the row-wise copy [rows, cols], or
+    with column=True the column-wise copy [cols, rows] (one per-tensor scale)."""
+    if column:
+        q, sf, s = qres["q_col"], qres["sf_col"], qres["s_col"]
+        rows, cols, per_row = qres["cols"], qres["rows"], 0
+    else:
+        q, sf, s = qres["q"], qres["sf"], qres["s"]
+        rows, cols, per_row = qres["rows"], qres["cols"], 1
+    y = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
+    nvfp4_dequantize(q, sf, s, per_row, rows, cols, y, y.stride(0), stream)
     return y
 
 
