@@ -76,6 +76,16 @@ def route_topk(rng, tokens, experts, topk):
     return np.ascontiguousarray(order[:, :topk].astype(np.int32))
 
 
+def topk_weights(seed, tokens, topk):
+    """Seeded combine weights [tokens, topk] (float32): positive, summing to about
+    one per token, in descending order like slots taken in descending logit
+    order.  Synthetic input data for the weighted combine."""
+    rng = np.random.default_rng(np.random.PCG64(1000 + seed))
+    e = np.exp(rng.standard_normal(size=(tokens, topk)))
+    e = -np.sort(-e, axis=1)
+    return np.ascontiguousarray((e / e.sum(axis=1, keepdims=True)).astype(np.float32))
+
+
 def moe_inputs(rng, tokens, hidden=2048, ffn=768, experts=128, topk=8, weights=True):
     topk_ids = route_topk(rng, tokens, experts, topk)
     x = to_bf16_bits(_normal(rng, (tokens, hidden)))

@@ -23,6 +23,9 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
   swiglu                         pinned (float64 closed form on exact inputs)
   dequantize_bf16                pinned (hand-worked values, exact binary64
                                  product within one bf16 rounding, round trip)
+  moe_combine                    pinned (top-1 unit weight = the inverse
+                                 permutation; exact dyadic sums; binary64 sum
+                                 within the binary32 bound; slot order)
 """
 import ctypes
 import os
@@ -64,6 +67,7 @@ def lib():
         L.orc_swiglu.argtypes = [P, I64, I64, I64, P]
         L.orc_bf16_from_double.argtypes = [P, I64, P]
         L.orc_dequantize_bf16.argtypes = [P, P, P, ctypes.c_int, I64, I64, P]
+        L.orc_moe_combine.argtypes = [P, I64, I64, P, P, I64, ctypes.c_int, I64, P]
         _lib = L
     return _lib
 
@@ -255,6 +259,19 @@ def moe_permute(topk_ids, num_experts, align=128, capacity=None):
     if rc != 0:
         raise ValueError("moe_permute: expert id out of range or capacity too small")
     return dict(offsets=offsets, gather=gather, dst=dst.reshape(T, k), capacity=cap)
+
+
+def moe_combine(y2_bf16, dst_rows, weights):
+    """out[t] = bf16(sum_j w[t, j] * y2[dst[t, j]]) in binary32, slot order."""
+    y2 = _c(y2_bf16, np.uint16)
+    dst = _c(dst_rows, np.int32).ravel()
+    w = _c(weights, np.float32)
+    tokens, topk = w.shape
+    assert dst.size == tokens * topk
+    rows, hidden = y2.shape
+    out = np.zeros((tokens, hidden), np.uint16)
+    lib().orc_moe_combine(_p(y2), rows, hidden, _p(dst), _p(w), tokens, topk, hidden, _p(out))
+    return out
 
 
 def swiglu(y1_bf16, F):

@@ -35,6 +35,9 @@
  *  R7  the column-wise copy quantizes X^T (16-blocks along tokens) with one
  *      per-tensor scale from the global amax.
  *  R9  swizzled scale-factor layout: 128 x 4 tiles of 512 bytes, row-tile major.
+ *  R11 dequantization to bf16 evaluates S * dec(s_b) * dec(q) in binary32 (the
+ *      product of the two codes is exact) and rounds the binary32 result to bf16.
+ *  R12 the routed-expert combine accumulates in binary32 in slot order.
  */
 #include <float.h>
 #include <math.h>
@@ -346,7 +349,7 @@ static uint16_t bf16_from_float_rne(float f) {
     return (uint16_t)upper;
 }
 
-/* Dequantization to bf16, the reading of the dequantized backward's input:
+/* Dequantization to bf16 (R11), the input of the dequantized backward:
  * c = dec(q) * dec(s_b) (exact in binary32), p = fl32(S * c), y = bf16_rn(p).
  * s_per_row == 0: s[0] for every row. */
 ORC_API void orc_dequantize_bf16(const uint8_t* q, const uint8_t* sf_rm, const float* s, int s_per_row,
@@ -578,6 +581,28 @@ ORC_API void orc_swiglu(const uint16_t* y1, int64_t rows, int64_t F, int64_t ld,
             double u = bf16_to_float(y1[r * ld + F + f]);
             double silu = g / (1.0 + exp(-g));
             h[r * F + f] = bf16_from_double(silu * u);
+        }
+}
+
+/* Unpermute + weighted combine after the expert GEMMs ([Miles], section on
+ * keeping shared experts in high precision: the sparsely selected routed
+ * experts' outputs pass through a high-precision weighted reduction).
+ * Reading R12: the reduction is binary32, in slot order, multiply then add:
+ * out[t, h] = bf16_rn(acc), acc = 0, then for j = 0 .. topk-1
+ * acc = fl32(acc + fl32(w[t, j] * y2[dst[t*topk + j], h])).  A dst row outside
+ * [0, rows) contributes nothing. */
+ORC_API void orc_moe_combine(const uint16_t* y2, int64_t rows, int64_t ld, const int32_t* dst,
+                             const float* w, int64_t tokens, int topk, int64_t hidden, uint16_t* out) {
+    for (int64_t t = 0; t < tokens; ++t)
+        for (int64_t h = 0; h < hidden; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < topk; ++j) {
+                int64_t r = dst[t * topk + j];
+                if (r < 0 || r >= rows) continue;
+                float prod = w[t * topk + j] * bf16_to_float(y2[r * ld + h]);
+                acc = acc + prod;
+            }
+            out[t * hidden + h] = bf16_from_float_rne(acc);
         }
 }
 
