@@ -270,6 +270,30 @@ NVFP4_API nvfp4_status nvfp4_grouped_gemm(
     void* y, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* Unpermute + weighted combine (after the MoE fc2)                          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * out[t, h] = bf16_rn( sum_{j < topk} w[t, j] * y2[dst_rows[t*topk + j], h] ),
+ * the routed experts' outputs brought back to token order and reduced with the
+ * router weights in high precision ("Towards Blackwell-Native 8-bit and 4-bit
+ * RL", shared-expert section): binary32, slot order j = 0..topk-1, each step
+ * one rounded multiply and one rounded add.  Bit-exact.
+ *
+ *  y2        bf16 [rows, ld_y2] (the fc2 output in the padded expert layout),
+ *            ld_y2 >= hidden, ld_y2 % 8 == 0, 16-byte aligned.
+ *  dst_rows  int32 [tokens * topk] on the device (nvfp4_moe_permute's dst_rows).
+ *            A row outside [0, rows) contributes nothing and sets the device
+ *            status to NVFP4_ERR_DEVICE_INPUT.
+ *  weights   float [tokens, topk] on the device.
+ *  topk      1..32.  hidden > 0, % 8 == 0.
+ *  out       bf16 [tokens, ld_out], ld_out >= hidden, ld_out % 8 == 0, 16-byte aligned.
+ */
+NVFP4_API nvfp4_status nvfp4_moe_combine(
+    const void* y2, int64_t rows, int64_t ld_y2, const int32_t* dst_rows, const float* weights,
+    int64_t tokens, int32_t topk, int64_t hidden, void* out, int64_t ld_out, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Dequantize (NVFP4 -> BF16)                                                */
 /* ------------------------------------------------------------------------- */
 

@@ -60,6 +60,7 @@ def lib():
         "nvfp4_grouped_gemm": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
         "nvfp4_swiglu_quantize": (st, [P, I64, I64, I64, P, P, P, P, P, P]),
         "nvfp4_dequantize": (st, [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]),
+        "nvfp4_moe_combine": (st, [P, I64, I64, P, P, I64, ctypes.c_int32, I64, P, I64, P]),
         "nvfp4_get_device_status": (st, [P]),
         "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "nvfp4_debug_cvt_probe": (st, [P, P, P, P]),
@@ -148,6 +149,12 @@ def nvfp4_grouped_gemm(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_
     _ok("nvfp4_grouped_gemm", lib().nvfp4_grouped_gemm(
         _p(a_q), _p(a_sf), _p(a_s), rows_capacity, _p(expert_offsets), E, _p(b_q), _p(b_sf),
         _p(b_s), N, K, _p(y), _s(stream)))
+
+
+def nvfp4_moe_combine(y2, rows, ld_y2, dst_rows, weights, tokens, topk, hidden, out, ld_out, stream=None):
+    _ok("nvfp4_moe_combine", lib().nvfp4_moe_combine(
+        _p(y2), rows, ld_y2, _p(dst_rows), _p(weights), tokens, int(topk), hidden, _p(out), ld_out,
+        _s(stream)))
 
 
 def nvfp4_dequantize(q, sf, s, s_per_row, rows, cols, y, ld_y, stream=None):
@@ -282,6 +289,16 @@ def grouped_gemm(a, expert_offsets, num_experts, b_q, b_sf, b_s, N, K, out=None,
     nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], rows, expert_offsets, num_experts, b_q, b_sf, b_s,
                        N, K, y, stream)
     return y
+
+
+def moe_combine(y2, dst_rows, weights, out=None, stream=None):
+    """bf16 [tokens, hidden]: sum_j weights[t, j] * y2[dst_rows[t, j]] (binary32, slot order)."""
+    tokens, topk = weights.shape
+    hidden = y2.shape[1]
+    o = out if out is not None else torch.empty((tokens, hidden), dtype=torch.bfloat16, device=y2.device)
+    nvfp4_moe_combine(y2, y2.shape[0], y2.stride(0), dst_rows, weights, tokens, topk, hidden, o, o.stride(0),
+                      stream)
+    return o
 
 
 def dequantize(qres, column=False, out=None, stream=None):
