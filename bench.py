@@ -337,6 +337,28 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 4 * args.steps,
         "wall_s_timed_loop": round(t_wall, 3),
     }
+    # NVFP4 -> bf16 dequantization of the same activation (the dequantized backward's input)
+    yx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dq = [lambda: ops.nvfp4_dequantize(qx["q"], qx["sf"], qx["s"], 1, M, K, yx, K, stream)]
+    for _ in range(3):
+        dq[0]()
+    torch.cuda.synchronize()
+    (gdq,) = capture_graphs(torch, dq, stream)
+    dq_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        gdq.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dq_ms.append(e0.elapsed_time(e1))
+    dq_t = float(np.mean(dq_ms))
+    dq_bytes = M * K * 0.5 + M * K / 16 + M * 4 + M * K * 2
+    result["dequantize"] = {"ms": round(dq_t, 5), "gbs": round(dq_bytes / (dq_t * 1e-3) / 1e9, 1),
+                            "frac_of_hbm": round(dq_bytes / (dq_t * 1e-3) / 1e9 / hbm_gbs, 4),
+                            "shape": [M, K]}
+    result["gpu_launches"] += args.steps
     if not args.no_moe:
         result["moe"] = run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs)
         result["gpu_launches"] += result["moe"].pop("launches")
@@ -378,6 +400,8 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
               sf=torch.empty(ops.nvfp4_sf_bytes(cap, F), dtype=torch.uint8, device=dev),
               s=torch.empty(cap, dtype=torch.float32, device=dev))
     y2 = torch.empty((cap, H), dtype=torch.bfloat16, device=dev)
+    cw = torch.from_numpy(W.topk_weights(2, T, k)).to(dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -392,6 +416,7 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
                                           stream),
         lambda: ops.nvfp4_grouped_gemm(hq["q"], hq["sf"], hq["s"], cap, off, E, w2["q"], w2["sf"],
                                        w2["s"], H, F, y2, stream),
+        lambda: ops.nvfp4_moe_combine(y2, cap, H, dst, cw, T, k, H, out, H, stream),
     ]
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -411,12 +436,13 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
     runs = []
     for _ in range(args.steps):
         flush.zero_()
-        evs = [ev() for _ in range(6)]
+        evs = [ev() for _ in range(len(stages) + 1)]
         step(evs)
         runs.append(evs)
     torch.cuda.synchronize()
-    seg = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in runs]).mean(axis=0)
-    total = float(np.array([e[0].elapsed_time(e[5]) for e in runs]).mean())
+    ns = len(stages)
+    seg = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(ns)] for e in runs]).mean(axis=0)
+    total = float(np.array([e[0].elapsed_time(e[ns]) for e in runs]).mean())
     routed = T * k
     flop = 2.0 * routed * H * 2 * F + 2.0 * routed * F * H
     fc1_flop = 2.0 * routed * H * 2 * F
@@ -432,7 +458,9 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
         "padded_rows": used_rows, "routed_rows": routed,
         "kernels_ms": {"permute": round(seg[0], 5), "gather_quantize": round(seg[1], 5),
                        "grouped_fc1": round(seg[2], 5), "swiglu_quantize": round(seg[3], 5),
-                       "grouped_fc2": round(seg[4], 5)},
+                       "grouped_fc2": round(seg[4], 5), "combine": round(seg[5], 5)},
+        # combine: reads top-k rows of the fc2 output per token, writes one row
+        "combine_gbs": round((routed * H * 2 + T * H * 2 + routed * 8) / (seg[5] * 1e-3) / 1e9, 1),
         "grouped_fc1": {"tflops": round(fc1_flop / (seg[2] * 1e-3) / 1e12, 1),
                         "frac_of_fp4_peak": round(fc1_flop / (seg[2] * 1e-3) / 1e12 / fp4_peak, 4),
                         "weight_gbs": round(w1_bytes / (seg[2] * 1e-3) / 1e9, 1),
@@ -441,7 +469,7 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
                         "frac_of_fp4_peak": round(fc2_flop / (seg[4] * 1e-3) / 1e12 / fp4_peak, 4),
                         "weight_gbs": round(w2_bytes / (seg[4] * 1e-3) / 1e9, 1),
                         "weight_frac_of_hbm": round(w2_bytes / (seg[4] * 1e-3) / 1e9 / hbm_gbs, 4)},
-        "launches": 7 * args.steps,
+        "launches": 8 * args.steps,
     }
 
 
