@@ -153,6 +153,27 @@ NVFP4_API nvfp4_status nvfp4_quantize_per_token(
     void* q_col, void* sf_col, float* s_col,
     void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/*
+ * Per-token quantization of a linear layer's two GEMM operands with the same
+ * K in one launch: x (an activation, optionally with its column-wise copy) and
+ * w (a weight, per output row).  Each tensor's bytes are exactly those of
+ * nvfp4_quantize_per_token on it alone (per-token scales make every row
+ * independent: "Towards Blackwell-Native 8-bit and 4-bit RL", "Online
+ * computation of the per-token scale").  One kernel walks the rows of both,
+ * so the two small quantizations share one ramp-up.
+ *
+ *  x, w           bf16 [rows_x, ld_x], [rows_w, ld_w]; 16-byte aligned, ld % 8 == 0.
+ *  q_x, sf_x, s_x and q_w, sf_w, s_w   as nvfp4_quantize_per_token's row outputs.
+ *  q_col, sf_col, s_col   all NULL, or x's column-wise copy (rows_x % 16 == 0;
+ *                 needs the workspace, nvfp4_quantize_workspace_bytes()).
+ *  cols           > 0, % 16 == 0.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_per_token_pair(
+    const void* x, int64_t rows_x, int64_t ld_x, void* q_x, void* sf_x, float* s_x,
+    void* q_col, void* sf_col, float* s_col,
+    const void* w, int64_t rows_w, int64_t ld_w, void* q_w, void* sf_w, float* s_w,
+    int64_t cols, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* MoE routing permute                                                       */
 /* ------------------------------------------------------------------------- */

@@ -96,8 +96,18 @@ __device__ __forceinline__ void bulk_row_load(void* dst, const void* src, uint32
         : "memory");
 }
 
+// Rows of up to two tensors with the same number of columns: row slots
+// [0, split) are tensor 0's rows and padding rows (rows_out .. rows_pad, whose
+// swizzled scale words are zeroed), [split, total) tensor 1's.  One launch
+// then quantizes, e.g., a linear layer's activation and its weight.
+struct RowJob {
+    RowParams t0, t1;
+    int64_t split;      // row slots of tensor 0
+    int64_t total;      // row slots of both
+};
+
 template <int NB, int MODE>
-__global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowParams p, StageCfg cfg) {
+__global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowJob job, StageCfg cfg) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -105,9 +115,10 @@ __global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowParams p, 
     uint8_t* bufs = smem + static_cast<size_t>(warp) * cfg.depth * cfg.row_pad;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(nwarps) * cfg.depth * cfg.row_pad) +
                      warp * cfg.depth;
-    const int nblocks = p.cols >> 4;
-    const uint32_t row_bytes = static_cast<uint32_t>(p.cols) * 2u;
-    const float tensor_amax = (MODE == kPerTensor) ? __uint_as_float(*p.amax_ws) : 0.0f;
+    const int nblocks = job.t0.cols >> 4;
+    const int kgroups = job.t0.kgroups;
+    const uint32_t row_bytes = static_cast<uint32_t>(job.t0.cols) * 2u;
+    const float tensor_amax = (MODE == kPerTensor) ? __uint_as_float(*job.t0.amax_ws) : 0.0f;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
     const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
 
@@ -117,41 +128,72 @@ __global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowParams p, 
     }
     __syncwarp();
 
-    // Start the copy of row r into buffer d (a zero row only completes the phase).
+    // source row of slot r (-1: a zero row or a padding row; no copy is issued)
+    auto source = [&](int64_t r) -> int64_t {
+        const bool sec = r >= job.split;
+        const int64_t lr = sec ? r - job.split : r;
+        const int64_t rows_out = sec ? job.t1.rows_out : job.t0.rows_out;
+        if (lr >= rows_out) return -1;
+        const int32_t* gather = sec ? job.t1.gather : job.t0.gather;
+        int64_t src = gather ? static_cast<int64_t>(gather[lr]) : lr;
+        if (src >= (sec ? job.t1.rows_in : job.t0.rows_in)) {
+            record_error(job.t0.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
+            src = -1;
+        }
+        return src;
+    };
+    // Start the copy of slot r into buffer d (a zero row only completes the phase).
     auto issue = [&](int64_t r, int d) {
-        if (r >= p.rows_out || lane != 0) return;
-        const int64_t src = source_row(p, r);
+        if (r >= job.total || lane != 0) return;
+        const int64_t src = source(r);
         if (src >= 0) {
+            const bool sec = r >= job.split;
+            const uint16_t* x = sec ? job.t1.x : job.t0.x;
+            const int64_t ld = sec ? job.t1.ld_x : job.t0.ld_x;
             mbar_arrive_expect_tx(&bars[d], row_bytes);
-            bulk_row_load(bufs + static_cast<size_t>(d) * cfg.row_pad, p.x + src * p.ld_x, row_bytes,
-                          &bars[d]);
+            bulk_row_load(bufs + static_cast<size_t>(d) * cfg.row_pad, x + src * ld, row_bytes, &bars[d]);
         } else {
             mbar_arrive(&bars[d]);
         }
     };
     for (int d = 0; d < cfg.depth; ++d) issue(first + d * stride, d);
 
-    float seen_amax = 0.0f;
+    float seen0 = 0.0f, seen1 = 0.0f;
     uint32_t parity = 0;   // bit d = phase parity expected next on buffer d
     int d = 0;
-    for (int64_t r = first; r < p.rows_out; r += stride) {
-        const int64_t src = p.gather ? static_cast<int64_t>(p.gather[r]) : r;
-        const bool zero_row = src < 0 || src >= p.rows_in;   // no copy was issued for it
+    for (int64_t r = first; r < job.total; r += stride) {
+        const bool sec = r >= job.split;
+        const int64_t lr = sec ? r - job.split : r;
+        const int64_t rows_out = sec ? job.t1.rows_out : job.t0.rows_out;
+        const bool pad_row = lr >= rows_out;
+        bool zero_row = pad_row;
+        if (!pad_row) {
+            const int32_t* gather = sec ? job.t1.gather : job.t0.gather;
+            const int64_t src = gather ? static_cast<int64_t>(gather[lr]) : lr;
+            zero_row = src < 0 || src >= (sec ? job.t1.rows_in : job.t0.rows_in);   // no copy was issued
+        }
         bool ok = mbar_wait_bounded(&bars[d], (parity >> d) & 1u, 2000000000ull, nullptr);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
             if (lane == 0) {
-                record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_NONE);
+                record_error(job.t0.status, NVFP4_ERR_TIMEOUT, DETAIL_NONE);
                 // let the copies this warp still has in flight land before it exits
                 for (int k = 0; k < cfg.depth; ++k) {
                     const int bb = (d + k) % cfg.depth;
-                    if (r + k * stride < p.rows_out)
+                    if (r + k * stride < job.total)
                         mbar_wait_bounded(&bars[bb], (parity >> bb) & 1u, 200000000ull, nullptr);
                 }
             }
             break;
         }
         parity ^= 1u << d;
+        if (pad_row) {
+            __syncwarp();
+            issue(r + cfg.depth * stride, d);
+            d = (d + 1 == cfg.depth) ? 0 : d + 1;
+            if (MODE != kAmaxOnly) zero_sf_row(sec ? job.t1.sf : job.t0.sf, kgroups, lr, lane);
+            continue;
+        }
         const uint4* row = reinterpret_cast<const uint4*>(bufs + static_cast<size_t>(d) * cfg.row_pad);
         Block16 v[NB];
 #pragma unroll
@@ -172,18 +214,17 @@ __global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowParams p, 
             row_amax = fmaxf(row_amax, bmax[i]);
         }
         row_amax = warp_max(row_amax);
-        seen_amax = fmaxf(seen_amax, row_amax);
+        if (sec) seen1 = fmaxf(seen1, row_amax);
+        else seen0 = fmaxf(seen0, row_amax);
         if (MODE == kAmaxOnly) continue;
-        encode_row_blocks<NB>(v, bmax, MODE == kPerTensor ? tensor_amax : row_amax, nblocks, p.kgroups,
-                              reinterpret_cast<uint2*>(p.q), p.sf, p.s, r, lane);
+        encode_row_blocks<NB>(v, bmax, MODE == kPerTensor ? tensor_amax : row_amax, nblocks, kgroups,
+                              reinterpret_cast<uint2*>(sec ? job.t1.q : job.t0.q), sec ? job.t1.sf : job.t0.sf,
+                              sec ? job.t1.s : job.t0.s, lr, lane);
     }
-    if (MODE != kAmaxOnly) {
-        // padding rows of the swizzled scales (rows_out .. rows_pad)
-        for (int64_t rp = p.rows_out + first; rp < p.rows_pad; rp += stride)
-            zero_sf_row(p.sf, p.kgroups, rp, lane);
+    if (MODE != kPerTensor && lane == 0) {
+        if (job.t0.amax_ws != nullptr && seen0 > 0.0f) atomicMax(job.t0.amax_ws, __float_as_uint(seen0));
+        if (job.t1.amax_ws != nullptr && seen1 > 0.0f) atomicMax(job.t1.amax_ws, __float_as_uint(seen1));
     }
-    if (MODE != kPerTensor && p.amax_ws != nullptr && lane == 0 && seen_amax > 0.0f)
-        atomicMax(p.amax_ws, __float_as_uint(seen_amax));
 }
 
 // Rows longer than 256 * 16 elements: two passes over the row (the second from L1/L2).
@@ -371,8 +412,7 @@ bool staged_config(int cols, int* warps, StageCfg* cfg) {
 }
 
 template <int NB, int MODE>
-nvfp4_status launch_staged(const RowParams& p, int warps, StageCfg cfg, const DeviceCtx& ctx,
-                           cudaStream_t s) {
+nvfp4_status launch_staged(const RowJob& job, int warps, StageCfg cfg, const DeviceCtx& ctx, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(warps) * cfg.depth * (cfg.row_pad + 8);
     static bool attr[64] = {};
     if (!attr[ctx.device & 63]) {
@@ -381,28 +421,44 @@ nvfp4_status launch_staged(const RowParams& p, int warps, StageCfg cfg, const De
             return NVFP4_ERR_CUDA;
         attr[ctx.device & 63] = true;
     }
-    const int64_t rows = (MODE == kAmaxOnly) ? p.rows_out : p.rows_pad;
-    const int64_t want = ceil_div(rows, warps);
+    const int64_t want = ceil_div(job.total, warps);
     const int grid = static_cast<int>(want < ctx.sm_count ? want : ctx.sm_count);
-    quant_rows_staged_kernel<NB, MODE><<<grid, warps * 32, smem, s>>>(p, cfg);
+    quant_rows_staged_kernel<NB, MODE><<<grid, warps * 32, smem, s>>>(job, cfg);
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;
 }
 
+// Staged path for a job (one or two tensors with the same columns); false if
+// the row does not fit the staged geometry (the caller falls back).
 template <int MODE>
-nvfp4_status launch_rows(const RowParams& p, int blocks, const DeviceCtx& ctx, cudaStream_t s) {
-    const int need = (p.cols / 8 + 31) / 32;
+bool try_launch_staged(const RowJob& job, const DeviceCtx& ctx, cudaStream_t s, nvfp4_status* st) {
     int warps = 0;
     StageCfg cfg{0, 0};
-    const int nb = (p.cols / 16 + 31) / 32;   // 16-element blocks per lane
-    if (nb <= 8 && staged_config(p.cols, &warps, &cfg)) {
-        if (nb <= 1) return launch_staged<1, MODE>(p, warps, cfg, ctx, s);
-        if (nb <= 2) return launch_staged<2, MODE>(p, warps, cfg, ctx, s);
-        if (nb <= 3) return launch_staged<3, MODE>(p, warps, cfg, ctx, s);
-        if (nb <= 4) return launch_staged<4, MODE>(p, warps, cfg, ctx, s);
-        if (nb <= 6) return launch_staged<6, MODE>(p, warps, cfg, ctx, s);
-        return launch_staged<8, MODE>(p, warps, cfg, ctx, s);
-    }
+    const int nb = (job.t0.cols / 16 + 31) / 32;   // 16-element blocks per lane
+    if (nb > 8 || !staged_config(job.t0.cols, &warps, &cfg)) return false;
+    if (nb <= 1) *st = launch_staged<1, MODE>(job, warps, cfg, ctx, s);
+    else if (nb <= 2) *st = launch_staged<2, MODE>(job, warps, cfg, ctx, s);
+    else if (nb <= 3) *st = launch_staged<3, MODE>(job, warps, cfg, ctx, s);
+    else if (nb <= 4) *st = launch_staged<4, MODE>(job, warps, cfg, ctx, s);
+    else if (nb <= 5) *st = launch_staged<5, MODE>(job, warps, cfg, ctx, s);
+    else if (nb <= 6) *st = launch_staged<6, MODE>(job, warps, cfg, ctx, s);
+    else *st = launch_staged<8, MODE>(job, warps, cfg, ctx, s);
+    return true;
+}
+
+template <int MODE>
+nvfp4_status launch_rows(const RowParams& p, int blocks, const DeviceCtx& ctx, cudaStream_t s) {
+    RowJob job;
+    job.t0 = p;
+    job.t1 = p;
+    job.t1.rows_out = 0;
+    job.t1.rows_pad = 0;
+    job.t1.amax_ws = nullptr;
+    job.split = (MODE == kAmaxOnly) ? p.rows_out : p.rows_pad;
+    job.total = job.split;
+    nvfp4_status st = NVFP4_OK;
+    if (try_launch_staged<MODE>(job, ctx, s, &st)) return st;
+    const int need = (p.cols / 8 + 31) / 32;
     if (need <= 1) quant_rows_kernel<1, MODE><<<blocks, kRowThreads, 0, s>>>(p);
     else if (need <= 2) quant_rows_kernel<2, MODE><<<blocks, kRowThreads, 0, s>>>(p);
     else if (need <= 4) quant_rows_kernel<4, MODE><<<blocks, kRowThreads, 0, s>>>(p);
@@ -415,6 +471,49 @@ nvfp4_status launch_rows(const RowParams& p, int blocks, const DeviceCtx& ctx, c
 }
 
 }  // namespace
+
+// Per-token rows of two tensors with the same columns in one launch (row
+// kernel's staged path; two launches when the row is too long for it).
+nvfp4_status quantize_rows_pair_launch(const RowParams& a, const RowParams& b, const DeviceCtx& ctx,
+                                       cudaStream_t s) {
+    RowJob job;
+    job.t0 = a;
+    job.t1 = b;
+    job.split = a.rows_pad;
+    job.total = a.rows_pad + b.rows_pad;
+    if (job.total == 0) return NVFP4_OK;
+    nvfp4_status st = NVFP4_OK;
+    if (try_launch_staged<kPerToken>(job, ctx, s, &st)) return st;
+    if (a.rows_pad > 0) {
+        const int64_t want = ceil_div(a.rows_pad, kRowThreads / 32);
+        st = launch_rows<kPerToken>(a, static_cast<int>(want < 1048576 ? want : 1048576), ctx, s);
+        if (st != NVFP4_OK) return st;
+    }
+    if (b.rows_pad > 0) {
+        const int64_t want = ceil_div(b.rows_pad, kRowThreads / 32);
+        st = launch_rows<kPerToken>(b, static_cast<int>(want < 1048576 ? want : 1048576), ctx, s);
+    }
+    return st;
+}
+
+RowParams row_params(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q, void* sf, float* s,
+                     unsigned* amax_ws, unsigned* status) {
+    RowParams p;
+    p.x = static_cast<const uint16_t*>(x);
+    p.rows_in = rows;
+    p.ld_x = ld;
+    p.gather = nullptr;
+    p.rows_out = rows;
+    p.rows_pad = round_up(rows, 128);
+    p.q = static_cast<uint32_t*>(q);
+    p.sf = static_cast<uint8_t*>(sf);
+    p.s = s;
+    p.amax_ws = amax_ws;
+    p.status = status;
+    p.cols = static_cast<int>(cols);
+    p.kgroups = static_cast<int>(round_up(cols / 16, 4) / 4);
+    return p;
+}
 
 // Shared by the ABI entry and by the SwiGLU file's requantize check.
 nvfp4_status quantize_rows_launch(const uint16_t* x, int64_t rows_in, int64_t cols, int64_t ld_x,
@@ -522,6 +621,45 @@ nvfp4_status nvfp4_quantize_per_token(const void* x, int64_t rows_in, int64_t co
     if (want_col)
         st = quantize_cols_launch(xb, rows_in, cols, ld_x, gather_rows, rows_out, q_col, sf_col,
                                   s_col, amax_ws, ctx, s);
+    return st;
+}
+
+nvfp4_status nvfp4_quantize_per_token_pair(const void* x, int64_t rows_x, int64_t ld_x, void* q_x,
+                                           void* sf_x, float* s_x, void* q_col, void* sf_col,
+                                           float* s_col, const void* w, int64_t rows_w, int64_t ld_w,
+                                           void* q_w, void* sf_w, float* s_w, int64_t cols,
+                                           void* workspace, size_t workspace_bytes,
+                                           nvfp4_stream_t stream) {
+    DeviceCtx ctx;
+    nvfp4_status st = device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
+    if (rows_x < 0 || rows_w < 0 || cols <= 0 || cols % 16 != 0 || cols > (int64_t(1) << 24))
+        return NVFP4_ERR_SHAPE;
+    if (ld_x < cols || ld_x % 8 != 0 || ld_w < cols || ld_w % 8 != 0) return NVFP4_ERR_SHAPE;
+    const bool want_col = (q_col != nullptr) || (sf_col != nullptr) || (s_col != nullptr);
+    if (want_col && (q_col == nullptr || sf_col == nullptr || s_col == nullptr)) return NVFP4_ERR_INVALID_ARG;
+    if (want_col && rows_x % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (rows_x > 0 && (x == nullptr || q_x == nullptr || sf_x == nullptr || s_x == nullptr))
+        return NVFP4_ERR_INVALID_ARG;
+    if (rows_w > 0 && (w == nullptr || q_w == nullptr || sf_w == nullptr || s_w == nullptr))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q_x, 16) || !aligned(sf_x, 16) || !aligned(s_x, 4) ||
+        !aligned(w, 16) || !aligned(q_w, 16) || !aligned(sf_w, 16) || !aligned(s_w, 4) ||
+        !aligned(q_col, 16) || !aligned(sf_col, 16) || !aligned(s_col, 4))
+        return NVFP4_ERR_ALIGNMENT;
+    if (want_col && (workspace == nullptr || workspace_bytes < nvfp4_quantize_workspace_bytes()))
+        return NVFP4_ERR_WORKSPACE;
+    if (want_col && !aligned(workspace, 4)) return NVFP4_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned* amax_ws = want_col ? static_cast<unsigned*>(workspace) : nullptr;
+    if (want_col && cudaMemsetAsync(amax_ws, 0, sizeof(unsigned), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+    const RowParams a = row_params(x, rows_x, cols, ld_x, q_x, sf_x, s_x, amax_ws, ctx.status);
+    const RowParams b = row_params(w, rows_w, cols, ld_w, q_w, sf_w, s_w, nullptr, ctx.status);
+    st = quantize_rows_pair_launch(a, b, ctx, s);
+    if (st != NVFP4_OK) return st;
+    if (want_col)
+        st = quantize_cols_launch(static_cast<const uint16_t*>(x), rows_x, cols, ld_x, nullptr, rows_x, q_col,
+                                  sf_col, s_col, amax_ws, ctx, s);
     return st;
 }
 

@@ -60,6 +60,8 @@ def lib():
         "nvfp4_grouped_gemm": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
         "nvfp4_swiglu_quantize": (st, [P, I64, I64, I64, P, P, P, P, P, P]),
         "nvfp4_dequantize": (st, [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]),
+        "nvfp4_quantize_per_token_pair": (st, [P, I64, I64, P, P, P, P, P, P, P, I64, I64, P, P, P, I64, P,
+                                               SZ, P]),
         "nvfp4_moe_combine": (st, [P, I64, I64, P, P, I64, ctypes.c_int32, I64, P, I64, P]),
         "nvfp4_get_device_status": (st, [P]),
         "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -157,6 +159,13 @@ def nvfp4_moe_combine(y2, rows, ld_y2, dst_rows, weights, tokens, topk, hidden, 
         _s(stream)))
 
 
+def nvfp4_quantize_per_token_pair(x, rows_x, ld_x, q_x, sf_x, s_x, q_col, sf_col, s_col, w, rows_w, ld_w,
+                                  q_w, sf_w, s_w, cols, workspace=None, workspace_bytes=0, stream=None):
+    _ok("nvfp4_quantize_per_token_pair", lib().nvfp4_quantize_per_token_pair(
+        _p(x), rows_x, ld_x, _p(q_x), _p(sf_x), _p(s_x), _p(q_col), _p(sf_col), _p(s_col), _p(w), rows_w, ld_w,
+        _p(q_w), _p(sf_w), _p(s_w), cols, _p(workspace), workspace_bytes, _s(stream)))
+
+
 def nvfp4_dequantize(q, sf, s, s_per_row, rows, cols, y, ld_y, stream=None):
     _ok("nvfp4_dequantize", lib().nvfp4_dequantize(
         _p(q), _p(sf), _p(s), int(s_per_row), rows, cols, _p(y), ld_y, _s(stream)))
@@ -247,6 +256,35 @@ def gemm(a, b, out=None, stream=None):
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a["q"].device)
     nvfp4_gemm(a["q"], a["sf"], a["s"], M, b["q"], b["sf"], b["s"], N, K, y, y.stride(0), stream)
     return y
+
+
+def quantize_pair(x, w, column_copy=False, workspace=None, stream=None):
+    """Per-token quantization of an activation x [rows_x, K] (optionally with its
+    column-wise copy) and a weight w [rows_w, K] in one launch; returns two
+    dicts shaped like quantize()'s."""
+    assert x.dtype == torch.bfloat16 and w.dtype == torch.bfloat16 and x.shape[1] == w.shape[1]
+    assert (x.shape[0] == 0 or x.stride(1) == 1) and (w.shape[0] == 0 or w.stride(1) == 1)
+    K = x.shape[1]
+    ld_x = x.stride(0) if x.shape[0] > 0 else K
+    ld_w = w.stride(0) if w.shape[0] > 0 else K
+    dev = x.device
+
+    def outs(rows):
+        return dict(rows=rows, cols=K, q=_u8((rows, K // 2), dev), sf=_u8(nvfp4_sf_bytes(rows, K), dev),
+                    s=torch.empty(rows, dtype=torch.float32, device=dev))
+    ox, ow = outs(x.shape[0]), outs(w.shape[0])
+    qc = sfc = sc = ws = None
+    wsb = 0
+    if column_copy:
+        qc = _u8((K, x.shape[0] // 2), dev)
+        sfc = _u8(nvfp4_sf_bytes(K, x.shape[0]), dev)
+        sc = torch.empty(1, dtype=torch.float32, device=dev)
+        ox.update(q_col=qc, sf_col=sfc, s_col=sc)
+        wsb = nvfp4_quantize_workspace_bytes()
+        ws = (workspace or Workspace(dev)).get(wsb)
+    nvfp4_quantize_per_token_pair(x, x.shape[0], ld_x, ox["q"], ox["sf"], ox["s"], qc, sfc, sc,
+                                  w, w.shape[0], ld_w, ow["q"], ow["sf"], ow["s"], K, ws, wsb, stream)
+    return ox, ow
 
 
 def moe_permute(topk_ids, num_experts, row_align=128, workspace=None, stream=None):
