@@ -353,6 +353,37 @@ def run_ours(args, rank, world, local_rank):
                             "frac_of_hbm": round(dq_bytes / (dq_t * 1e-3) / 1e9 / hbm_gbs, 4),
                             "shape": [M, K]}
     result["gpu_launches"] += args.steps
+    # NVFP4 backward GEMMs on the same layer (column-wise copies, one scale each):
+    # dgrad dX = dY W and wgrad dW = dY^T X; dY is a synthetic gradient [M, N]
+    dy = to_dev(W.small_matrix(77, M, N, std=1e-3))
+    qdy = ops.quantize(dy, column_copy=True)
+    qwc = ops.quantize(w, column_copy=True)
+    qxc = ops.quantize(x, column_copy=True)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    bw = [lambda: ops.gemm_dgrad(qdy, qwc, out=dx, stream=stream),
+          lambda: ops.gemm_wgrad(qdy, qxc, out=dw, stream=stream)]
+    for _ in range(3):
+        for fn in bw:
+            fn()
+    torch.cuda.synchronize()
+    gbw = capture_graphs(torch, bw, stream)
+    bw_ms = [[], []]
+    for _ in range(args.steps):
+        for i, g in enumerate(gbw):
+            flush.zero_()
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            bw_ms[i].append(e0.elapsed_time(e1))
+    t_dg, t_wg = float(np.mean(bw_ms[0])), float(np.mean(bw_ms[1]))
+    result["backward"] = {"dgrad_ms": round(t_dg, 5), "wgrad_ms": round(t_wg, 5),
+                          "dgrad_tflops": round(flop / (t_dg * 1e-3) / 1e12, 1),
+                          "wgrad_tflops": round(flop / (t_wg * 1e-3) / 1e12, 1),
+                          "shapes": {"dgrad": [M, K, N], "wgrad": [N, K, M]}}
+    result["gpu_launches"] += 2 * args.steps
     if not args.no_moe:
         result["moe"] = run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs)
         result["gpu_launches"] += result["moe"].pop("launches")

@@ -263,6 +263,25 @@ NVFP4_API nvfp4_status nvfp4_gemm(
     void* y, int64_t ld_y, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_gemm with a choice of outer-scale granularity per operand:
+ * a_s_per_row / b_s_per_row != 0 read S_a[m] / S_b[n] from arrays as above;
+ * == 0 read one scale a_s[0] / b_s[0] for every row -- the column-wise copies'
+ * single per-tensor scale.  This makes the NVFP4 backward GEMMs ("Towards
+ * Blackwell-Native 8-bit and 4-bit RL", "Backward activation representation
+ * trade-off" and the backward modes; the pages' recipe itself runs these in
+ * BF16):
+ *   dgrad  dX[M, K]  = dY[M, N] W[N, K]:   A = dY (rows, per token),
+ *                      B = W's column-wise copy [K, N] (one scale);
+ *   wgrad  dW[N, K]  = dY^T X:             A = dY's column-wise copy [N, M],
+ *                      B = X's column-wise copy [K, M] (one scale each).
+ * Shapes and alignment as nvfp4_gemm (the contraction length K % 64 == 0).
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_ex(
+    const void* a_q, const void* a_sf, const float* a_s, int32_t a_s_per_row, int64_t M,
+    const void* b_q, const void* b_sf, const float* b_s, int32_t b_s_per_row, int64_t N, int64_t K,
+    void* y, int64_t ld_y, nvfp4_stream_t stream);
+
+/*
  * Grouped (MoE) W4A4 GEMM: for every expert e, rows m in
  * [expert_offsets[e], expert_offsets[e+1]) of A are multiplied by expert e's
  * weights:  Y[m, n] = bf16_rn( S_a[m] * S_b[e, n] * sum_k dec(a)[m,k] dec(b_e)[n,k] ).

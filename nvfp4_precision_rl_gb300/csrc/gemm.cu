@@ -86,6 +86,8 @@ struct GemmParams {
     int num_n_tiles;
     int num_m_tiles;          // dense: ceil(M / 128); grouped: capacity tiles
     int E;                    // grouped: experts; dense: 0
+    int sa_stride;            // 1: S_a per row of A; 0: one S_a for all rows
+    int sb_stride;            // 1: S_b per row of B; 0: one S_b for all rows
 };
 
 // ----------------------------------------------------------------------------
@@ -665,14 +667,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const bool write = tl.m_base + rank * 128 < tl.row_end;
             const int64_t row0 = tl.m_base + rank * 128 + quad * 32;
             const int64_t m = row0 + lane;
-            const float sa = (m < p.M) ? __ldg(p.sa + m) : 0.0f;
+            const float sa = (m < p.M) ? __ldg(p.sa + m * p.sa_stride) : 0.0f;
             const int64_t n_half = tl.n0 + half * (kBN / 2);
-            const float* sbp = p.sb + (kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half;
+            const float* sbp =
+                p.sb + p.sb_stride * ((kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half);
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < kBN / 2 / 32; ++i) {
                 const int64_t n = n_half + i * 32 + lane;
-                sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + i * 32 + lane) : 0.0f;
+                sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + (i * 32 + lane) * p.sb_stride) : 0.0f;
             }
             __syncwarp();
             bool ok = mbar_wait_cluster(acc_full, acc_phase, kWaitLimitNs, abort_flag);
@@ -846,9 +849,10 @@ using namespace nvfp4;
 
 extern "C" {
 
-nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int64_t M,
-                        const void* b_q, const void* b_sf, const float* b_s, int64_t N, int64_t K,
-                        void* y, int64_t ld_y, nvfp4_stream_t stream) {
+nvfp4_status nvfp4_gemm_ex(const void* a_q, const void* a_sf, const float* a_s, int32_t a_s_per_row,
+                           int64_t M, const void* b_q, const void* b_sf, const float* b_s,
+                           int32_t b_s_per_row, int64_t N, int64_t K, void* y, int64_t ld_y,
+                           nvfp4_stream_t stream) {
     DeviceCtx ctx;
     nvfp4_status st = device_ctx(&ctx);
     if (st != NVFP4_OK) return st;
@@ -882,9 +886,17 @@ nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int
     p.num_n_tiles = static_cast<int>(ceil_div(N, kBN));
     p.num_m_tiles = static_cast<int>(ceil_div(M, kBM));
     p.E = 0;
+    p.sa_stride = a_s_per_row ? 1 : 0;
+    p.sb_stride = b_s_per_row ? 1 : 0;
     const int64_t pair_tiles = ceil_div(M, 256) * p.num_n_tiles;
     if (pair_tiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
     return launch_gemm_pair<false>(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int64_t M,
+                        const void* b_q, const void* b_sf, const float* b_s, int64_t N, int64_t K,
+                        void* y, int64_t ld_y, nvfp4_stream_t stream) {
+    return nvfp4_gemm_ex(a_q, a_sf, a_s, 1, M, b_q, b_sf, b_s, 1, N, K, y, ld_y, stream);
 }
 
 nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* a_s,
@@ -925,6 +937,8 @@ nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* 
     p.num_n_tiles = static_cast<int>(ceil_div(N, kBN));
     p.num_m_tiles = static_cast<int>(ceil_div(rows_capacity, kBM));
     p.E = E;
+    p.sa_stride = 1;
+    p.sb_stride = 1;
     // slots: every 128-row tile of the capacity x every n-tile (about half start a pair tile)
     const int64_t slots = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     if (slots > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;

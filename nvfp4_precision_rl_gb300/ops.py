@@ -60,6 +60,7 @@ def lib():
         "nvfp4_grouped_gemm": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
         "nvfp4_swiglu_quantize": (st, [P, I64, I64, I64, P, P, P, P, P, P]),
         "nvfp4_dequantize": (st, [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]),
+        "nvfp4_gemm_ex": (st, [P, P, P, ctypes.c_int32, I64, P, P, P, ctypes.c_int32, I64, I64, P, I64, P]),
         "nvfp4_quantize_per_token_pair": (st, [P, I64, I64, P, P, P, P, P, P, P, I64, I64, P, P, P, I64, P,
                                                SZ, P]),
         "nvfp4_moe_combine": (st, [P, I64, I64, P, P, I64, ctypes.c_int32, I64, P, I64, P]),
@@ -164,6 +165,12 @@ def nvfp4_quantize_per_token_pair(x, rows_x, ld_x, q_x, sf_x, s_x, q_col, sf_col
     _ok("nvfp4_quantize_per_token_pair", lib().nvfp4_quantize_per_token_pair(
         _p(x), rows_x, ld_x, _p(q_x), _p(sf_x), _p(s_x), _p(q_col), _p(sf_col), _p(s_col), _p(w), rows_w, ld_w,
         _p(q_w), _p(sf_w), _p(s_w), cols, _p(workspace), workspace_bytes, _s(stream)))
+
+
+def nvfp4_gemm_ex(a_q, a_sf, a_s, a_s_per_row, M, b_q, b_sf, b_s, b_s_per_row, N, K, y, ld_y, stream=None):
+    _ok("nvfp4_gemm_ex", lib().nvfp4_gemm_ex(
+        _p(a_q), _p(a_sf), _p(a_s), int(a_s_per_row), M, _p(b_q), _p(b_sf), _p(b_s), int(b_s_per_row), N, K,
+        _p(y), ld_y, _s(stream)))
 
 
 def nvfp4_dequantize(q, sf, s, s_per_row, rows, cols, y, ld_y, stream=None):
@@ -285,6 +292,33 @@ def quantize_pair(x, w, column_copy=False, workspace=None, stream=None):
     nvfp4_quantize_per_token_pair(x, x.shape[0], ld_x, ox["q"], ox["sf"], ox["s"], qc, sfc, sc,
                                   w, w.shape[0], ld_w, ow["q"], ow["sf"], ow["s"], K, ws, wsb, stream)
     return ox, ow
+
+
+def _operand(qres, column):
+    if column:
+        return qres["q_col"], qres["sf_col"], qres["s_col"], 0, qres["cols"], qres["rows"]
+    return qres["q"], qres["sf"], qres["s"], 1, qres["rows"], qres["cols"]
+
+
+def gemm_ex(a, b, a_column=False, b_column=False, out=None, stream=None):
+    """Y = A B^T where A / B is a quantize() result's row-wise copy, or with
+    *_column=True its column-wise copy (transposed operand, one outer scale)."""
+    aq, asf, as_, apr, M, K = _operand(a, a_column)
+    bq, bsf, bs, bpr, N, Kb = _operand(b, b_column)
+    assert K == Kb
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    nvfp4_gemm_ex(aq, asf, as_, apr, M, bq, bsf, bs, bpr, N, K, y, y.stride(0), stream)
+    return y
+
+
+def gemm_dgrad(dy, w, out=None, stream=None):
+    """dX [M, K] = dY [M, N] W [N, K]: dY's rows x W's column-wise copy."""
+    return gemm_ex(dy, w, b_column=True, out=out, stream=stream)
+
+
+def gemm_wgrad(dy, x, out=None, stream=None):
+    """dW [N, K] = dY^T X: dY's and X's column-wise copies."""
+    return gemm_ex(dy, x, a_column=True, b_column=True, out=out, stream=stream)
 
 
 def moe_permute(topk_ids, num_experts, row_align=128, workspace=None, stream=None):
