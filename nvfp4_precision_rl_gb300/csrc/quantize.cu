@@ -655,7 +655,9 @@ nvfp4_status nvfp4_quantize_per_token_pair(const void* x, int64_t rows_x, int64_
     if (want_col && cudaMemsetAsync(amax_ws, 0, sizeof(unsigned), s) != cudaSuccess) return NVFP4_ERR_CUDA;
     const RowParams a = row_params(x, rows_x, cols, ld_x, q_x, sf_x, s_x, amax_ws, ctx.status);
     const RowParams b = row_params(w, rows_w, cols, ld_w, q_w, sf_w, s_w, nullptr, ctx.status);
-    st = quantize_rows_pair_launch(a, b, ctx, s);
+    // the weight's rows first, the activation's last: its column-wise copy (the
+    // next kernel) then re-reads it from L2 rather than HBM
+    st = quantize_rows_pair_launch(b, a, ctx, s);
     if (st != NVFP4_OK) return st;
     if (want_col)
         st = quantize_cols_launch(static_cast<const uint16_t*>(x), rows_x, cols, ld_x, nullptr, rows_x, q_col,
