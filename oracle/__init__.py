@@ -23,6 +23,9 @@ Parity status per function (what pins it is in tests/test_oracle_*.py):
   swiglu                         pinned (float64 closed form on exact inputs)
   dequantize_bf16                pinned (hand-worked values, exact binary64
                                  product within one bf16 rounding, round trip)
+  mxfp8_quantize / dequantize    pinned (hand-worked blocks, the rounded-up
+                                 scale's minimality, torch float8_e4m3fn
+                                 codec, exact dequantization, round trip)
   moe_combine                    pinned (top-1 unit weight = the inverse
                                  permutation; exact dyadic sums; binary64 sum
                                  within the binary32 bound; slot order)
@@ -68,6 +71,9 @@ def lib():
         L.orc_bf16_from_double.argtypes = [P, I64, P]
         L.orc_dequantize_bf16.argtypes = [P, P, P, ctypes.c_int, I64, I64, P]
         L.orc_moe_combine.argtypes = [P, I64, I64, P, P, I64, ctypes.c_int, I64, P]
+        L.orc_mxfp8_quantize_rows.argtypes = [P, I64, I64, I64, P, P]
+        L.orc_mxfp8_quantize_cols.argtypes = [P, I64, I64, I64, P, P]
+        L.orc_mxfp8_dequantize_bf16.argtypes = [P, P, I64, I64, P]
         _lib = L
     return _lib
 
@@ -259,6 +265,33 @@ def moe_permute(topk_ids, num_experts, align=128, capacity=None):
     if rc != 0:
         raise ValueError("moe_permute: expert id out of range or capacity too small")
     return dict(offsets=offsets, gather=gather, dst=dst.reshape(T, k), capacity=cap)
+
+
+def mxfp8_quantize(x_bf16, column_copy=False):
+    """MXFP8 of bf16 [rows, cols]: q [rows, cols] E4M3 codes, sf [rows, cols/32]
+    E8M0 codes (row-major) and sf_swz (the 128 x 4 tile layout); with
+    column_copy the 32x1 copy of X^T: q_col [cols, rows], sf_col, sf_col_swz."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    q = np.zeros((rows, cols), np.uint8)
+    sf = np.zeros((rows, cols // 32), np.uint8)
+    lib().orc_mxfp8_quantize_rows(_p(x), rows, cols, cols, _p(q), _p(sf))
+    out = dict(q=q, sf=sf, sf_swz=sf_swizzle(sf))
+    if column_copy:
+        qc = np.zeros((cols, rows), np.uint8)
+        sfc = np.zeros((cols, rows // 32), np.uint8)
+        lib().orc_mxfp8_quantize_cols(_p(x), rows, cols, cols, _p(qc), _p(sfc))
+        out.update(q_col=qc, sf_col=sfc, sf_col_swz=sf_swizzle(sfc))
+    return out
+
+
+def mxfp8_dequantize_bf16(q, sf_rm):
+    q = _c(q, np.uint8)
+    sf_rm = _c(sf_rm, np.uint8)
+    rows, cols = q.shape
+    out = np.zeros((rows, cols), np.uint16)
+    lib().orc_mxfp8_dequantize_bf16(_p(q), _p(sf_rm), rows, cols, _p(out))
+    return out
 
 
 def moe_combine(y2_bf16, dst_rows, weights):

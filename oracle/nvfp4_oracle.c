@@ -38,6 +38,8 @@
  *  R11 dequantization to bf16 evaluates S * dec(s_b) * dec(q) in binary32 (the
  *      product of the two codes is exact) and rounds the binary32 result to bf16.
  *  R12 the routed-expert combine accumulates in binary32 in slot order.
+ *  R13 MXFP8 scale: the smallest power of two 2^e (e >= -127) with
+ *      448 * 2^e >= amax_b; elements E4M3(x / 2^e), ties to even, sign kept.
  */
 #include <float.h>
 #include <math.h>
@@ -603,6 +605,76 @@ ORC_API void orc_moe_combine(const uint16_t* y2, int64_t rows, int64_t ld, const
                 acc = acc + prod;
             }
             out[t * hidden + h] = bf16_from_float_rne(acc);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8 ([Miles] "MXFP8 format background": 1x32 blocks of E4M3 values      */
+/* sharing one E8M0 power-of-two scale, rounded up so that the block maximum */
+/* is not clipped; row-wise 1x32 and column-wise 32x1 copies are quantized   */
+/* independently from the full-precision data, "Backward activation         */
+/* representation trade-off").                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Reading R13: the scale is 2^e with e the smallest integer >= -127 such that
+ * 448 * 2^e >= amax_b (amax_b = 0 gives -127); E8M0 code = e + 127. */
+static int mx_exponent(float amax) {
+    int e = -127;
+    while (ldexp(448.0, e) < (double)amax) ++e;
+    return e;
+}
+
+/* E4M3 of x / 2^e, nearest with ties to the even code, saturating, sign kept. */
+static uint8_t mx_element(float x, int e) {
+    double v = ldexp((double)x, -e);                 /* exact */
+    int sign = signbit(x) ? 0x80 : 0;
+    return (uint8_t)(sign | nearest_code(fabs(v), g_e4m3, 127));
+}
+
+/* Rows: q [rows, cols] E4M3 codes, sf_rm [rows, cols/32] E8M0 codes. */
+ORC_API void orc_mxfp8_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q,
+                                     uint8_t* sf_rm) {
+    tables();
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = fabsf(bf16_to_float(x[r * ld + b * 32 + i]));
+                if (a > amax) amax = a;
+            }
+            int e = mx_exponent(amax);
+            sf_rm[r * (cols / 32) + b] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i)
+                q[r * cols + b * 32 + i] = mx_element(bf16_to_float(x[r * ld + b * 32 + i]), e);
+        }
+}
+
+/* Columns (X^T, 32x1 blocks along the rows): q [cols, rows], sf_rm [cols, rows/32]. */
+ORC_API void orc_mxfp8_quantize_cols(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q,
+                                     uint8_t* sf_rm) {
+    tables();
+    for (int64_t k = 0; k < cols; ++k)
+        for (int64_t b = 0; b < rows / 32; ++b) {
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = fabsf(bf16_to_float(x[(b * 32 + i) * ld + k]));
+                if (a > amax) amax = a;
+            }
+            int e = mx_exponent(amax);
+            sf_rm[k * (rows / 32) + b] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i)
+                q[k * rows + b * 32 + i] = mx_element(bf16_to_float(x[(b * 32 + i) * ld + k]), e);
+        }
+}
+
+/* bf16 of dec(q) * 2^(code - 127), one rounding of the exact product. */
+ORC_API void orc_mxfp8_dequantize_bf16(const uint8_t* q, const uint8_t* sf_rm, int64_t rows, int64_t cols,
+                                       uint16_t* out) {
+    tables();
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < cols; ++k) {
+            double v = g_e4m3[q[r * cols + k]] * ldexp(1.0, (int)sf_rm[r * (cols / 32) + k / 32] - 127);
+            out[r * cols + k] = bf16_from_double(v);
         }
 }
 
