@@ -353,6 +353,36 @@ def run_ours(args, rank, world, local_rank):
                             "frac_of_hbm": round(dq_bytes / (dq_t * 1e-3) / 1e9 / hbm_gbs, 4),
                             "shape": [M, K]}
     result["gpu_launches"] += args.steps
+    # MXFP8 of the same activation: 1x32 row copy + 32x1 column copy, then the
+    # row copy dequantized back to bf16
+    mx = ops.mxfp8_quantize(x, column_copy=True)
+    ymx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    mxs = [lambda: ops.nvfp4_mxfp8_quantize(x, M, K, K, mx["q"], mx["sf"], mx["q_col"], mx["sf_col"], stream),
+           lambda: ops.nvfp4_mxfp8_dequantize(mx["q"], mx["sf"], M, K, ymx, K, stream)]
+    for _ in range(3):
+        for fn in mxs:
+            fn()
+    torch.cuda.synchronize()
+    gmx = capture_graphs(torch, mxs, stream)
+    mx_ms = [[], []]
+    for _ in range(args.steps):
+        for i, g in enumerate(gmx):
+            flush.zero_()
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            mx_ms[i].append(e0.elapsed_time(e1))
+    t_mq, t_md = float(np.mean(mx_ms[0])), float(np.mean(mx_ms[1]))
+    mq_bytes = M * K * 2 + 2 * (M * K + M * K / 32)     # read X once; both copies written
+    md_bytes = M * K + M * K / 32 + M * K * 2
+    result["mxfp8"] = {"quantize_row_col_ms": round(t_mq, 5),
+                       "quantize_gbs": round(mq_bytes / (t_mq * 1e-3) / 1e9, 1),
+                       "dequantize_ms": round(t_md, 5),
+                       "dequantize_gbs": round(md_bytes / (t_md * 1e-3) / 1e9, 1),
+                       "shape": [M, K]}
+    result["gpu_launches"] += 3 * args.steps
     # NVFP4 backward GEMMs on the same layer (column-wise copies, one scale each):
     # dgrad dX = dY W and wgrad dW = dY^T X; dY is a synthetic gradient [M, N]
     dy = to_dev(W.small_matrix(77, M, N, std=1e-3))

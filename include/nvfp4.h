@@ -359,6 +359,51 @@ NVFP4_API nvfp4_status nvfp4_dequantize(
     void* y, int64_t ld_y, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* MXFP8 (E4M3 values, E8M0 scale per 32 values)                             */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of a swizzled E8M0 scale array for [rows, cols]: the 128 x 4 tile
+ * layout of nvfp4_sf_bytes with one byte per 32 values,
+ * round_up(rows, 128) * round_up(ceil(cols / 32), 4); 0 when either is <= 0. */
+NVFP4_API size_t nvfp4_mxfp8_sf_bytes(int64_t rows, int64_t cols);
+
+/*
+ * MXFP8 quantization ("Towards Blackwell-Native 8-bit and 4-bit RL", MXFP8
+ * format background; "Backward activation representation trade-off"): each
+ * 1x32 block of a row shares the scale 2^e, e the smallest integer >= -127
+ * with 448 * 2^e >= the block's amax (stored as the E8M0 code e + 127); each
+ * value is E4M3_RNE_satfinite(x * 2^-e), the product exact.  With q_col/sf_col
+ * the same is done for the 32x1 blocks of each column, stored as X^T.
+ * Bit-exact.
+ *
+ *  x       bf16 [rows, ld_x], ld_x >= cols, ld_x % 8 == 0, 16-byte aligned.
+ *  cols    > 0, % 32 == 0.
+ *  q       E4M3 codes [rows, cols] (device, 16-byte aligned).
+ *  sf      swizzled E8M0 codes, nvfp4_mxfp8_sf_bytes(rows, cols) bytes; the
+ *          padding is zeroed.
+ *  q_col   NULL, or E4M3 codes of X^T [cols, rows] (16-byte aligned); needs
+ *          rows % 32 == 0.
+ *  sf_col  swizzled E8M0 codes of X^T, nvfp4_mxfp8_sf_bytes(cols, rows) bytes;
+ *          NULL exactly when q_col is.
+ *  Errors: NVFP4_ERR_SHAPE / _ALIGNMENT / _INVALID_ARG; rows == 0 is a no-op.
+ */
+NVFP4_API nvfp4_status nvfp4_mxfp8_quantize(
+    const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q, void* sf, void* q_col, void* sf_col,
+    nvfp4_stream_t stream);
+
+/*
+ * y[r, k] = bf16_rn( dec(q[r, k]) * 2^(code - 127) ), the product exact in
+ * binary32 (E8M0 code 0 is 2^-127).  Bit-exact.
+ *
+ *  q       E4M3 codes [rows, cols], 16-byte aligned;  sf  swizzled E8M0 codes.
+ *  cols    > 0, % 32 == 0.
+ *  y       bf16 [rows, ld_y], ld_y >= cols, ld_y % 8 == 0, 16-byte aligned.
+ *  Errors: NVFP4_ERR_SHAPE / _ALIGNMENT / _INVALID_ARG; rows == 0 is a no-op.
+ */
+NVFP4_API nvfp4_status nvfp4_mxfp8_dequantize(
+    const void* q, const void* sf, int64_t rows, int64_t cols, void* y, int64_t ld_y, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* SwiGLU + requantize (the MoE fc2 input)                                   */
 /* ------------------------------------------------------------------------- */
 

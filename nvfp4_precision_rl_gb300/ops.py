@@ -64,6 +64,9 @@ def lib():
         "nvfp4_quantize_per_token_pair": (st, [P, I64, I64, P, P, P, P, P, P, P, I64, I64, P, P, P, I64, P,
                                                SZ, P]),
         "nvfp4_moe_combine": (st, [P, I64, I64, P, P, I64, ctypes.c_int32, I64, P, I64, P]),
+        "nvfp4_mxfp8_sf_bytes": (SZ, [I64, I64]),
+        "nvfp4_mxfp8_quantize": (st, [P, I64, I64, I64, P, P, P, P, P]),
+        "nvfp4_mxfp8_dequantize": (st, [P, P, I64, I64, P, I64, P]),
         "nvfp4_get_device_status": (st, [P]),
         "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "nvfp4_debug_cvt_probe": (st, [P, P, P, P]),
@@ -176,6 +179,20 @@ def nvfp4_gemm_ex(a_q, a_sf, a_s, a_s_per_row, M, b_q, b_sf, b_s, b_s_per_row, N
 def nvfp4_dequantize(q, sf, s, s_per_row, rows, cols, y, ld_y, stream=None):
     _ok("nvfp4_dequantize", lib().nvfp4_dequantize(
         _p(q), _p(sf), _p(s), int(s_per_row), rows, cols, _p(y), ld_y, _s(stream)))
+
+
+def nvfp4_mxfp8_sf_bytes(rows, cols):
+    return int(lib().nvfp4_mxfp8_sf_bytes(rows, cols))
+
+
+def nvfp4_mxfp8_quantize(x, rows, cols, ld_x, q, sf, q_col=None, sf_col=None, stream=None):
+    _ok("nvfp4_mxfp8_quantize", lib().nvfp4_mxfp8_quantize(
+        _p(x), rows, cols, ld_x, _p(q), _p(sf), _p(q_col), _p(sf_col), _s(stream)))
+
+
+def nvfp4_mxfp8_dequantize(q, sf, rows, cols, y, ld_y, stream=None):
+    _ok("nvfp4_mxfp8_dequantize", lib().nvfp4_mxfp8_dequantize(
+        _p(q), _p(sf), rows, cols, _p(y), ld_y, _s(stream)))
 
 
 def nvfp4_swiglu_quantize(y1, rows, ffn, ld_y1, row_count, q, sf, s, h=None, stream=None):
@@ -384,6 +401,31 @@ def dequantize(qres, column=False, out=None, stream=None):
         rows, cols, per_row = qres["rows"], qres["cols"], 1
     y = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
     nvfp4_dequantize(q, sf, s, per_row, rows, cols, y, y.stride(0), stream)
+    return y
+
+
+def mxfp8_quantize(x, column_copy=False, stream=None):
+    """MXFP8 of bf16 x [rows, cols]: q [rows, cols] E4M3 codes (uint8) and the
+    swizzled E8M0 scales sf; with column_copy also q_col [cols, rows] and
+    sf_col, the 32x1-block copy of X^T."""
+    rows, cols = x.shape
+    dev = x.device
+    out = dict(rows=rows, cols=cols, q=_u8((rows, cols), dev), sf=_u8(nvfp4_mxfp8_sf_bytes(rows, cols), dev))
+    if column_copy:
+        out.update(q_col=_u8((cols, rows), dev), sf_col=_u8(nvfp4_mxfp8_sf_bytes(cols, rows), dev))
+    nvfp4_mxfp8_quantize(x, rows, cols, x.stride(0), out["q"], out["sf"], out.get("q_col"), out.get("sf_col"),
+                         stream)
+    return out
+
+
+def mxfp8_dequantize(qres, column=False, out=None, stream=None):
+    """bf16 values of an mxfp8_quantize() result (column=True: the X^T copy)."""
+    if column:
+        q, sf, rows, cols = qres["q_col"], qres["sf_col"], qres["cols"], qres["rows"]
+    else:
+        q, sf, rows, cols = qres["q"], qres["sf"], qres["rows"], qres["cols"]
+    y = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
+    nvfp4_mxfp8_dequantize(q, sf, rows, cols, y, y.stride(0), stream)
     return y
 
 

@@ -54,6 +54,10 @@ def test_size_helpers_without_gpu(libpath):
     lib.nvfp4_moe_capacity.restype = ctypes.c_int64
     lib.nvfp4_moe_capacity.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
     assert lib.nvfp4_sf_bytes(300, 160) == 384 * 12
+    lib.nvfp4_mxfp8_sf_bytes.restype = ctypes.c_size_t
+    lib.nvfp4_mxfp8_sf_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert lib.nvfp4_mxfp8_sf_bytes(300, 160) == 384 * 8
+    assert lib.nvfp4_mxfp8_sf_bytes(130, 2080) == 256 * 68
     assert lib.nvfp4_packed_bytes(300, 160) == 300 * 80
     cap = lib.nvfp4_moe_capacity(4096, 8, 128, 128)
     assert cap % 128 == 0 and cap >= 4096 * 8 + 128 * 127
