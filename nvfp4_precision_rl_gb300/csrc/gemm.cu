@@ -427,16 +427,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int pair = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
     const int num_pm = static_cast<int>((p.M + 255) / 256);
-    int tiles = num_pm * p.num_n_tiles;
-    if (kGrouped) {
-        // slots of the padded layout in use: it ends at offsets[E]
-        int64_t used = __ldg(p.offsets + p.E);
-        if (used > p.M || used < 0) {
-            if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
-            used = used < 0 ? 0 : p.M;
-        }
-        tiles = static_cast<int>((used + 127) / 128) * p.num_n_tiles;
-    }
     const int a_row_tiles = static_cast<int>((p.M + 127) / 128);
     const int sfb_tiles_n = static_cast<int>((p.N + 127) / 128);
 
@@ -463,6 +453,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     cluster_sync_all();     // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    pdl_wait();             // the producers of the operands and offsets have completed
+    int tiles = num_pm * p.num_n_tiles;
+    if (kGrouped) {
+        // slots of the padded layout in use: it ends at offsets[E]
+        int64_t used = __ldg(p.offsets + p.E);
+        if (used > p.M || used < 0) {
+            if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
+            used = used < 0 ? 0 : p.M;
+        }
+        tiles = static_cast<int>((used + 127) / 128) * p.num_n_tiles;
+    }
 
     if ((warp == 0 || warp == kPBWarp) && lane < kPLoadLanes) {
         // ------------------------------ producers (both CTAs) ------------------
@@ -831,8 +832,20 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
     const int64_t cap = resident[ctx.device & 63];
     const int64_t pairs = pair_tiles < cap ? pair_tiles : cap;
     if (pairs <= 0) return NVFP4_OK;
-    nvfp4_gemm_pair_kernel<kGrouped><<<static_cast<int>(2 * pairs), kPThreads, kPSmemBytes, s>>>(ma, mb, my, p);
-    NVFP4_CHECK_LAUNCH();
+    // programmatic serialization: set-up (barriers, TMEM, tensor maps) overlaps
+    // the producer kernel's tail; the kernel waits before reading its inputs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(kPThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_pair_kernel<kGrouped>, ma, mb, my, p) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
     return NVFP4_OK;
 }
 

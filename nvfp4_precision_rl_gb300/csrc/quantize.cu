@@ -47,6 +47,7 @@ __device__ __forceinline__ int64_t source_row(const RowParams& p, int64_t r) {
 // Row kernel with the row held in registers: NCH chunks of 8 per lane (cols <= 256 * NCH).
 template <int NCH, int MODE>
 __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(RowParams p) {
+    pdl_launch_dependents();    // a dependent waits for this grid's completion itself
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kRowThreads / 32);
@@ -109,6 +110,7 @@ struct RowJob {
 template <int NB, int MODE>
 __global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowJob job, StageCfg cfg) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();    // a dependent waits for this grid's completion itself
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -230,6 +232,7 @@ __global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowJob job, S
 // Rows longer than 256 * 16 elements: two passes over the row (the second from L1/L2).
 template <int MODE>
 __global__ void __launch_bounds__(kRowThreads) quant_rows_long_kernel(RowParams p) {
+    pdl_launch_dependents();    // a dependent waits for this grid's completion itself
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kRowThreads / 32);
@@ -326,6 +329,8 @@ __device__ __forceinline__ uint2 encode_col_block(const uint32_t* v, float r) {
 // as two 16-byte stores when the row pitch allows it.
 template <bool kGather>
 __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
+    pdl_wait();                 // the row pass's amax (and any producer of x / gather)
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int k0 = blockIdx.x * 64 + lane * 2;
@@ -565,8 +570,20 @@ nvfp4_status quantize_cols_launch(const uint16_t* x, int64_t rows_in, int64_t co
     }
     dim3 grid(static_cast<unsigned>(round_up(cols, 128) / 64),
               static_cast<unsigned>(ceil_div(p.kgroups, kColThreads / 32)));
-    if (gather != nullptr) quant_cols_kernel<true><<<grid, kColThreads, 0, stream>>>(p);
-    else quant_cols_kernel<false><<<grid, kColThreads, 0, stream>>>(p);
+    // programmatic serialization: the kernel may start while the row pass
+    // finishes; it waits (griddepcontrol.wait) before reading anything
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kColThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = (gather != nullptr) ? cudaLaunchKernelEx(&cfg, quant_cols_kernel<true>, p)
+                                              : cudaLaunchKernelEx(&cfg, quant_cols_kernel<false>, p);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;
 }

@@ -38,6 +38,7 @@ __device__ __forceinline__ uint32_t swiglu_pair(uint32_t g2, uint32_t u2) {
 
 template <int NCH>
 __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(SwiParams p) {
+    pdl_launch_dependents();    // a dependent waits for this grid's completion itself
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
