@@ -15,24 +15,26 @@
 // memory (128 each) and whose 256 B rows are split 128/128 between them; each
 // CTA holds its own 128 x 256 FP32 accumulator in TMEM.  Persistent: one pair
 // per two SMs, tiles strided over the pairs.  Per CTA, warp-specialised:
-//   warp 0 / warp 14  TMA producers (A and its scales / this CTA's B rows and
+//   warp 0 / warp 2  TMA producers (A and its scales / this CTA's B rows and
 //               the B scales) into a 5-stage shared-memory ring; two issuing
 //               threads because one thread's TMA copies are processed serially.
 //   warp 1      TMEM allocation (collective across the pair); in the even CTA
 //               the MMA issuer: warp-uniform loop, one elected lane issues the
 //               MMAs and the multicast commits that release both CTAs' stages.
-//   warps 2..5  scale warps, one per TMEM lane quadrant: each reads the stage's
+//   warps 4..7  scale warps, one per TMEM lane quadrant: each reads the stage's
 //               512-byte scale atoms from shared memory (line = lane) and writes
 //               them into its own 32 TMEM lanes with tcgen05.st -- the same
 //               4-way replicated image a tcgen05.cp 32x128b.warpx4 would make,
 //               but on the warps' TMEM store path, which (measured) overlaps the
 //               MMAs, whereas every tcgen05.cp occupies the serial MMA pipe --
 //               then arrive on the even CTA's barrier.
-//   warps 6..13 epilogue, two warps per TMEM lane quadrant (128 columns each):
-//               tcgen05.ld 64 columns at a time, scale by S_a * S_b with packed
-//               FP32x2 multiplies, round to bf16, stage in 128-byte swizzled
-//               shared memory and store with TMA; the accumulator is released
-//               after the second load, before any store.
+//   warps 8..15 epilogue, two warps per TMEM lane quadrant (128 columns each):
+//               tcgen05.ld all 128 columns in one round, release the
+//               accumulator, then scale by S_a * S_b with packed FP32x2
+//               multiplies, round to bf16, stage in 128-byte swizzled shared
+//               memory and store with TMA.  setmaxnreg moves registers from the
+//               producer / MMA and scale warpgroups (56 and 80 per thread) to
+//               the epilogue warpgroups (184), which hold the 128 columns.
 // Tile 256 x 256 per pair, K step of 256 FP4 = 128 bytes = one swizzle row.
 // The grouped (MoE) variant walks the padded per-expert layout (128-row
 // aligned segments, device-side offsets): a pair tile covers two 128-row tiles
@@ -56,7 +58,12 @@ constexpr int kBKBytes = 128;                // 256 FP4 values per K step
 constexpr int kMmaPerStage = 4;              // K = 64 per tcgen05.mma
 constexpr int kSFWarps = 4;                  // one per TMEM lane quadrant
 constexpr int kEpiWarps = 8;                 // two per TMEM lane quadrant, 128 columns each
-constexpr int kFirstSFWarp = 2;
+// Warp roles, aligned to warpgroups (setmaxnreg acts per warpgroup):
+//   warpgroup 0: warp 0 A producer, warp 1 TMEM allocation + MMA issuer (even
+//                CTA), warp 2 B producer, warp 3 idle;
+//   warpgroup 1: warps 4..7 scale warps; warpgroups 2 and 3: epilogue.
+constexpr int kPBWarp = 2;                   // the B-side producer
+constexpr int kFirstSFWarp = 4;
 constexpr int kFirstEpiWarp = kFirstSFWarp + kSFWarps;
 constexpr uint32_t kATileBytes = kBM * kBKBytes;      // 16 KB
 constexpr uint32_t kSFAtomBytes = 512;                // 128 rows x 4 scales
@@ -241,8 +248,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 //   MMA commits            -> empty / acc_full of both CTAs (multicast commit),
 //   epilogue (both CTAs)   -> acc_empty of the even CTA (remote arrive).
 constexpr int kPStages = 5;
-constexpr int kPBWarp = kFirstEpiWarp + kEpiWarps;                // the B-side producer
-constexpr int kPThreads = 32 * (kPBWarp + 1);
+constexpr int kPThreads = 32 * (kFirstEpiWarp + kEpiWarps);       // 512
+// Registers per thread after the split: the CTA launches with 128 per thread
+// (65,536 in all); warpgroups 0 and 1 give theirs up so the epilogue warps can
+// hold a whole 128-column half of the accumulator.  The sum must stay within
+// the launch's total, or setmaxnreg.inc would wait for registers forever.
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsWG0 = 56;
+constexpr int kRegsWG1 = 80;
+constexpr int kRegsEpi = 184;
+static_assert(kPThreads == 512, "four warpgroups");
+static_assert(128 * kRegsWG0 + 128 * kRegsWG1 + 256 * kRegsEpi <= kPThreads * kRegsLaunch,
+              "register split exceeds the launch's registers");
+static_assert(kRegsWG0 % 8 == 0 && kRegsWG1 % 8 == 0 && kRegsEpi % 8 == 0, "setmaxnreg granularity");
 constexpr int kPLoadLanes = 1;                                    // issuing lanes per producer warp
 constexpr unsigned kPLoadMask = (1u << kPLoadLanes) - 1;
 constexpr int kPBoxRows = 128 / kPLoadLanes;                      // rows of A or B per TMA box
@@ -465,286 +483,295 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         tiles = static_cast<int>((used + 127) / 128) * p.num_n_tiles;
     }
 
-    if ((warp == 0 || warp == kPBWarp) && lane < kPLoadLanes) {
-        // ------------------------------ producers (both CTAs) ------------------
-        // Warp 0 loads A and its scales, warp kPBWarp this CTA's 128 rows of B
-        // and the B scales; kPLoadLanes lanes of each split the rows.  TMA
-        // copies issued by one thread are processed one after another (about
-        // 27 bytes per SM clock for 16 KB tiles), so a stage fills at the rate
-        // of its issuing threads.  (Two warps with one lane each measured
-        // fastest: 64-row boxes from two lanes each were slower.)
-        const bool side_b = warp == kPBWarp;
-        const int sub = lane;                     // which kPBoxRows-row part
-        const CUtensorMap* map = side_b ? &tma_b : &tma_a;
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-        uint32_t stage = 0, phase = 0;
-        uint32_t issued_mask = 0, last_phase = 0;
-        bool ok = true;
-        for (int t = pair; t < tiles && ok; t += npairs) {
-            const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
-            if (!tl.run) continue;
-            if (kGrouped && !side_b && rank == 0 && (__ldg(p.offsets + tl.expert) & 127) != 0)
-                record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
-            const int64_t m0 = tl.m_base + rank * 128;
-            const int64_t n0 = tl.n0;
-            const int a_tile = static_cast<int>(m0 / 128);
-            const bool a_sf_ok = a_tile < a_row_tiles;
-            const int nt128 = static_cast<int>(n0 / 128);
-            const bool two_b_atoms = nt128 + 1 < sfb_tiles_n;
-            const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
-            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                ok = __all_sync(kPLoadMask,
-                                mbar_wait_cluster(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag));
-                if (!ok) break;
-                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
-                const uint32_t sf_bytes = ng * kSFAtomBytes;
-                const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
-                // lane 0 announces the side's bytes before any of its copies is issued
-                if (sub == 0)
-                    mbar_arrive_expect_tx(&full[stage], side_b ? kPBHalfBytes + (two_b_atoms ? 2u : 1u) * sf_bytes
-                                                               : kATileBytes + (a_sf_ok ? sf_bytes : 0u));
-                __syncwarp(kPLoadMask);
-                if (!side_b) {
-                    tma_load_2d(map, &full[stage], sA + stage * kATileBytes + sub * kPBoxRows * kBKBytes,
-                                kt * kBKBytes, static_cast<int32_t>(m0 + kPBoxRows * sub));
-                    if (a_sf_ok && sub == 0)
-                        bulk_load(sSFA + stage * kSFATileBytes,
-                                  p.sfa + (static_cast<int64_t>(a_tile) * p.kgroups + g0) * kSFAtomBytes,
-                                  sf_bytes, &full[stage]);
-                } else {
-                    tma_load_2d(map, &full[stage], sB + stage * kPBHalfBytes + sub * kPBoxRows * kBKBytes,
-                                kt * kBKBytes, static_cast<int32_t>(tl.b_row0 + rank * 128 + kPBoxRows * sub));
-                    if (sub == 0) {
-                        bulk_load(sSFB + stage * kSFBTileBytes,
-                                  sfb_e + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
-                                  &full[stage]);
-                        if (two_b_atoms)
-                            bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
-                                      sfb_e + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
+    // Roles by warpgroup.  Each branch starts with its warpgroup's register
+    // split (every warp of the warpgroup executes it, converged), so the code
+    // of the branch is compiled within that register count.
+    if (warp < kFirstSFWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG0));
+        if ((warp == 0 || warp == kPBWarp) && lane < kPLoadLanes) {
+            // ------------------------------ producers (both CTAs) ------------------
+            // Warp 0 loads A and its scales, warp kPBWarp this CTA's 128 rows of B
+            // and the B scales; kPLoadLanes lanes of each split the rows.  TMA
+            // copies issued by one thread are processed one after another (about
+            // 27 bytes per SM clock for 16 KB tiles), so a stage fills at the rate
+            // of its issuing threads.  (Two warps with one lane each measured
+            // fastest: 64-row boxes from two lanes each were slower.)
+            const bool side_b = warp == kPBWarp;
+            const int sub = lane;                     // which kPBoxRows-row part
+            const CUtensorMap* map = side_b ? &tma_b : &tma_a;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_mask = 0, last_phase = 0;
+            bool ok = true;
+            for (int t = pair; t < tiles && ok; t += npairs) {
+                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
+                if (!tl.run) continue;
+                if (kGrouped && !side_b && rank == 0 && (__ldg(p.offsets + tl.expert) & 127) != 0)
+                    record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
+                const int64_t m0 = tl.m_base + rank * 128;
+                const int64_t n0 = tl.n0;
+                const int a_tile = static_cast<int>(m0 / 128);
+                const bool a_sf_ok = a_tile < a_row_tiles;
+                const int nt128 = static_cast<int>(n0 / 128);
+                const bool two_b_atoms = nt128 + 1 < sfb_tiles_n;
+                const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
+                for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                    ok = __all_sync(kPLoadMask,
+                                    mbar_wait_cluster(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag));
+                    if (!ok) break;
+                    const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                    const uint32_t sf_bytes = ng * kSFAtomBytes;
+                    const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
+                    // lane 0 announces the side's bytes before any of its copies is issued
+                    if (sub == 0)
+                        mbar_arrive_expect_tx(&full[stage], side_b ? kPBHalfBytes + (two_b_atoms ? 2u : 1u) * sf_bytes
+                                                                   : kATileBytes + (a_sf_ok ? sf_bytes : 0u));
+                    __syncwarp(kPLoadMask);
+                    if (!side_b) {
+                        tma_load_2d(map, &full[stage], sA + stage * kATileBytes + sub * kPBoxRows * kBKBytes,
+                                    kt * kBKBytes, static_cast<int32_t>(m0 + kPBoxRows * sub));
+                        if (a_sf_ok && sub == 0)
+                            bulk_load(sSFA + stage * kSFATileBytes,
+                                      p.sfa + (static_cast<int64_t>(a_tile) * p.kgroups + g0) * kSFAtomBytes,
                                       sf_bytes, &full[stage]);
-                    }
-                }
-                issued_mask |= 1u << stage;
-                last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == kPStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            if (sub == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
-        }
-        // every copy this thread issued must land before the CTA may exit
-        for (int s = 0; s < kPStages; ++s)
-            if (issued_mask & (1u << s))
-                if (!mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kDrainLimitNs, nullptr))
-                    record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
-    } else if (warp == 1 && leader) {
-        // ------------------------------ MMA issuer (even CTA) ------------------
-        // The whole warp runs the loop (warp-uniform control flow and
-        // descriptors); one elected lane issues the MMAs and commits.
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
-        bool ok = true;
-        const uint64_t a_desc0 = sw128_desc(sA);
-        const uint64_t b_desc0 = sw128_desc(sB);
-        for (int t = pair; t < tiles && ok; t += npairs) {
-            if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                // both CTAs' scale warps have seen their stage full and written TMEM
-                ok = __all_sync(0xFFFFFFFFu,
-                                mbar_wait_cluster(&sf_ready[stage], phase, kWaitLimitNs, abort_flag));
-                if (!ok) break;
-                tc_fence_after();
-                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
-                const uint32_t sf_col = tmem + kSFTmemCol + stage * kSFTmemPerStage;
-                // descriptor start addresses advance in 16-byte units: 32 bytes per K step
-                const uint64_t ad = a_desc0 + stage * (kATileBytes >> 4);
-                const uint64_t bd = b_desc0 + stage * (kPBHalfBytes >> 4);
-                if (elect_one()) {
-                    if (ng == kMmaPerStage) {
-#pragma unroll
-                        for (int j = 0; j < kMmaPerStage; ++j)
-                            tc_mma_pair(tmem, ad + 2 * j, bd + 2 * j, (kt > 0 || j > 0) ? 1u : 0u,
-                                        sf_col + j * 4, sf_col + 16 + j * 8);
                     } else {
-                        for (int j = 0; j < ng; ++j)
-                            tc_mma_pair(tmem, ad + 2 * j, bd + 2 * j, (kt > 0 || j > 0) ? 1u : 0u,
-                                        sf_col + j * 4, sf_col + 16 + j * 8);
+                        tma_load_2d(map, &full[stage], sB + stage * kPBHalfBytes + sub * kPBoxRows * kBKBytes,
+                                    kt * kBKBytes, static_cast<int32_t>(tl.b_row0 + rank * 128 + kPBoxRows * sub));
+                        if (sub == 0) {
+                            bulk_load(sSFB + stage * kSFBTileBytes,
+                                      sfb_e + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
+                                      &full[stage]);
+                            if (two_b_atoms)
+                                bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
+                                          sfb_e + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
+                                          sf_bytes, &full[stage]);
+                        }
                     }
-                    tc_commit_pair_both(&empty[stage]);
-                }
-                __syncwarp();
-                if (++stage == kPStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (!ok) break;
-            if (elect_one()) tc_commit_pair_both(acc_full);
-            __syncwarp();
-            acc_phase ^= 1u;
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
-        }
-        // all tensor-core work issued by this warp completes before TMEM is freed
-        if (elect_one()) tc_commit_pair(drain);
-        __syncwarp();
-        if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr) && lane == 0)
-            record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
-    } else if (warp >= kFirstSFWarp && warp < kFirstEpiWarp) {
-        // ------------------------------ scale warps (both CTAs) ----------------
-        const int quad = warp & 3;
-        const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-        uint32_t stage = 0, phase = 0;
-        bool ok = true;
-        for (int t = pair; t < tiles && ok; t += npairs) {
-            if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
-            for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
-                got = __all_sync(0xFFFFFFFFu, got);
-                if (!got) {
-                    ok = false;
-                    break;
-                }
-                const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
-                const uint4* sfa_s = reinterpret_cast<const uint4*>(sSFA + stage * kSFATileBytes);
-                const uint4* sfb_s = reinterpret_cast<const uint4*>(sSFB + stage * kSFBTileBytes);
-                uint32_t va[16], vb[32];
-#pragma unroll
-                for (int j = 0; j < kMmaPerStage; ++j) {
-                    const uint4 a = (j < ng) ? sfa_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 b0 = (j < ng) ? sfb_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 b1 = (j < ng) ? sfb_s[(kSFATileBytes / 16) + j * 32 + lane]
-                                              : make_uint4(0u, 0u, 0u, 0u);
-                    va[4 * j] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
-                    vb[8 * j] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
-                    vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z;
-                    vb[8 * j + 7] = b1.w;
-                }
-                const uint32_t sf_col = tmem + t_lane + kSFTmemCol + stage * kSFTmemPerStage;
-                tmem_st16(sf_col, va);
-                tmem_st32(sf_col + 16, vb);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(peer_addr(&sf_ready[stage], 0));
-                if (++stage == kPStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                    issued_mask |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
-        }
-    } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kEpiWarps) {
-        // ------------------------------ epilogue (both CTAs) -------------------
-        // Warp (quad, half) owns TMEM lanes quad*32.. and accumulator columns
-        // half*128..: two rounds of 64 columns, each loaded with two tcgen05.ld
-        // and one wait, scaled by S_a[m] S_b[n], rounded to bf16, written into
-        // this warp's swizzled 32 x 64 staging box and stored by TMA (which
-        // clips rows >= M and columns >= N).
-        const int quad = warp & 3;
-        const int ew = warp - kFirstEpiWarp;
-        const int half = ew >> 2;
-        const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
-        float* sb_s = sSB + ew * (kBN / 2);
-        uint8_t* box = sOut + ew * kPOutBoxBytes;
-        uint8_t* my_row = box + lane * 128;
-        const uint32_t acc_empty_leader = peer_addr(acc_empty, 0);
-        uint32_t acc_phase = 0;
-        for (int t = pair; t < tiles; t += npairs) {
-            const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
-            if (!tl.run) continue;
-            // this CTA's 128 rows lie inside the tile's row range, or wholly past it
-            const bool write = tl.m_base + rank * 128 < tl.row_end;
-            const int64_t row0 = tl.m_base + rank * 128 + quad * 32;
-            const int64_t m = row0 + lane;
-            const float sa = (m < p.M) ? __ldg(p.sa + m * p.sa_stride) : 0.0f;
-            const int64_t n_half = tl.n0 + half * (kBN / 2);
-            const float* sbp =
-                p.sb + p.sb_stride * ((kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half);
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < kBN / 2 / 32; ++i) {
-                const int64_t n = n_half + i * 32 + lane;
-                sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + (i * 32 + lane) * p.sb_stride) : 0.0f;
-            }
-            __syncwarp();
-            bool ok = mbar_wait_cluster(acc_full, acc_phase, kWaitLimitNs, abort_flag);
-            ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) {
                 *abort_flag = 1;
-                if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_EPILOGUE);
-                break;
+                if (sub == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_PRODUCER);
             }
-            tc_fence_after();
-            // Staging of 64 packed columns (one round): wait until the previous
-            // store from this warp's box has read it, write the rows, then
-            // (separately) fence and store the box with TMA.
-            auto stage = [&](const uint32_t (&q)[16], const uint32_t (&q2)[16]) {
-                if (lane == 0) bulk_wait_read();
-                __syncwarp();
-                // 16-byte chunk j of row `lane` goes to chunk j ^ (lane % 8) (128-byte swizzle)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(q[4 * j], q[4 * j + 1], q[4 * j + 2], q[4 * j + 3]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(my_row + (((j + 4) ^ (lane & 7)) << 4)) =
-                        make_uint4(q2[4 * j], q2[4 * j + 1], q2[4 * j + 2], q2[4 * j + 3]);
-            };
-            auto store = [&](int64_t x) {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && write && row0 < p.M && x < p.N) {
-                    tma_store_2d(&tma_y, box, static_cast<int32_t>(x), static_cast<int32_t>(row0));
-                    bulk_commit();
+            // every copy this thread issued must land before the CTA may exit
+            for (int s = 0; s < kPStages; ++s)
+                if (issued_mask & (1u << s))
+                    if (!mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kDrainLimitNs, nullptr))
+                        record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
+        } else if (warp == 1 && leader) {
+            // ------------------------------ MMA issuer (even CTA) ------------------
+            // The whole warp runs the loop (warp-uniform control flow and
+            // descriptors); one elected lane issues the MMAs and commits.
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            bool ok = true;
+            const uint64_t a_desc0 = sw128_desc(sA);
+            const uint64_t b_desc0 = sw128_desc(sB);
+            for (int t = pair; t < tiles && ok; t += npairs) {
+                if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                    // both CTAs' scale warps have seen their stage full and written TMEM
+                    ok = __all_sync(0xFFFFFFFFu,
+                                    mbar_wait_cluster(&sf_ready[stage], phase, kWaitLimitNs, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                    const uint32_t sf_col = tmem + kSFTmemCol + stage * kSFTmemPerStage;
+                    // descriptor start addresses advance in 16-byte units: 32 bytes per K step
+                    const uint64_t ad = a_desc0 + stage * (kATileBytes >> 4);
+                    const uint64_t bd = b_desc0 + stage * (kPBHalfBytes >> 4);
+                    if (elect_one()) {
+                        if (ng == kMmaPerStage) {
+    #pragma unroll
+                            for (int j = 0; j < kMmaPerStage; ++j)
+                                tc_mma_pair(tmem, ad + 2 * j, bd + 2 * j, (kt > 0 || j > 0) ? 1u : 0u,
+                                            sf_col + j * 4, sf_col + 16 + j * 8);
+                        } else {
+                            for (int j = 0; j < ng; ++j)
+                                tc_mma_pair(tmem, ad + 2 * j, bd + 2 * j, (kt > 0 || j > 0) ? 1u : 0u,
+                                            sf_col + j * 4, sf_col + 16 + j * 8);
+                        }
+                        tc_commit_pair_both(&empty[stage]);
+                    }
+                    __syncwarp();
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-            };
-            // Round 0 is scaled and staged before round 1 is loaded, so the
-            // accumulator is released after two TMEM round trips and one round
-            // of arithmetic; the rest of the tile's output work follows.
-            {
-                uint32_t r0[32], r1[32], qa[16], qb[16];
+                if (!ok) break;
+                if (elect_one()) tc_commit_pair_both(acc_full);
+                __syncwarp();
+                acc_phase ^= 1u;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
+            }
+            // all tensor-core work issued by this warp completes before TMEM is freed
+            if (elect_one()) tc_commit_pair(drain);
+            __syncwarp();
+            if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr) && lane == 0)
+                record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
+        }
+    } else if (warp < kFirstEpiWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG1));
+            // ------------------------------ scale warps (both CTAs) ----------------
+            const int quad = warp & 3;
+            const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int t = pair; t < tiles && ok; t += npairs) {
+                if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
+                for (int kt = 0; kt < p.num_k_tiles; ++kt) {
+                    bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
+                    got = __all_sync(0xFFFFFFFFu, got);
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                    const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
+                    const uint4* sfa_s = reinterpret_cast<const uint4*>(sSFA + stage * kSFATileBytes);
+                    const uint4* sfb_s = reinterpret_cast<const uint4*>(sSFB + stage * kSFBTileBytes);
+                    uint32_t va[16], vb[32];
+    #pragma unroll
+                    for (int j = 0; j < kMmaPerStage; ++j) {
+                        const uint4 a = (j < ng) ? sfa_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 b0 = (j < ng) ? sfb_s[j * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 b1 = (j < ng) ? sfb_s[(kSFATileBytes / 16) + j * 32 + lane]
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+                        va[4 * j] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
+                        vb[8 * j] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
+                        vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z;
+                        vb[8 * j + 7] = b1.w;
+                    }
+                    const uint32_t sf_col = tmem + t_lane + kSFTmemCol + stage * kSFTmemPerStage;
+                    tmem_st16(sf_col, va);
+                    tmem_st32(sf_col + 16, vb);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(peer_addr(&sf_ready[stage], 0));
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
+            }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+            // ------------------------------ epilogue (both CTAs) -------------------
+            // Warp (quad, half) owns TMEM lanes quad*32.. and accumulator columns
+            // half*128..: two rounds of 64 columns, each loaded with two tcgen05.ld
+            // and one wait, scaled by S_a[m] S_b[n], rounded to bf16, written into
+            // this warp's swizzled 32 x 64 staging box and stored by TMA (which
+            // clips rows >= M and columns >= N).
+            const int quad = warp & 3;
+            const int ew = warp - kFirstEpiWarp;
+            const int half = ew >> 2;
+            const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
+            float* sb_s = sSB + ew * (kBN / 2);
+            uint8_t* box = sOut + ew * kPOutBoxBytes;
+            uint8_t* my_row = box + lane * 128;
+            const uint32_t acc_empty_leader = peer_addr(acc_empty, 0);
+            uint32_t acc_phase = 0;
+            for (int t = pair; t < tiles; t += npairs) {
+                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
+                if (!tl.run) continue;
+                // this CTA's 128 rows lie inside the tile's row range, or wholly past it
+                const bool write = tl.m_base + rank * 128 < tl.row_end;
+                const int64_t row0 = tl.m_base + rank * 128 + quad * 32;
+                const int64_t m = row0 + lane;
+                const float sa = (m < p.M) ? __ldg(p.sa + m * p.sa_stride) : 0.0f;
+                const int64_t n_half = tl.n0 + half * (kBN / 2);
+                const float* sbp =
+                    p.sb + p.sb_stride * ((kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half);
+                __syncwarp();
+    #pragma unroll
+                for (int i = 0; i < kBN / 2 / 32; ++i) {
+                    const int64_t n = n_half + i * 32 + lane;
+                    sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + (i * 32 + lane) * p.sb_stride) : 0.0f;
+                }
+                __syncwarp();
+                bool ok = mbar_wait_cluster(acc_full, acc_phase, kWaitLimitNs, abort_flag);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) {
+                    *abort_flag = 1;
+                    if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_EPILOGUE);
+                    break;
+                }
+                tc_fence_after();
+                // Staging of 64 packed columns (one round): wait until the previous
+                // store from this warp's box has read it, write the rows, then
+                // (separately) fence and store the box with TMA.
+                auto stage = [&](const uint32_t (&q)[16], const uint32_t (&q2)[16]) {
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+                    // 16-byte chunk j of row `lane` goes to chunk j ^ (lane % 8) (128-byte swizzle)
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(my_row + ((j ^ (lane & 7)) << 4)) =
+                            make_uint4(q[4 * j], q[4 * j + 1], q[4 * j + 2], q[4 * j + 3]);
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(my_row + (((j + 4) ^ (lane & 7)) << 4)) =
+                            make_uint4(q2[4 * j], q2[4 * j + 1], q2[4 * j + 2], q2[4 * j + 3]);
+                };
+                auto store = [&](int64_t x) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && write && row0 < p.M && x < p.N) {
+                        tma_store_2d(&tma_y, box, static_cast<int32_t>(x), static_cast<int32_t>(row0));
+                        bulk_commit();
+                    }
+                };
+                // The warp's 128 accumulator columns are loaded in one round and the
+                // accumulator released at once; scaling, staging and the stores
+                // (two 64-column boxes) follow while the next tile's MMAs run.
+                uint32_t r0[32], r1[32], r2[32], r3[32];
                 tmem_ld32(t_base, r0);
                 tmem_ld32(t_base + 32, r1);
+                tmem_ld32(t_base + 64, r2);
+                tmem_ld32(t_base + 96, r3);
                 tmem_wait(r0);
                 reg_fence(r1);
-                scale_chunk(r0, sb_s, sa, qa);
-                scale_chunk(r1, sb_s + 32, sa, qb);
-                stage(qa, qb);
-            }
-            {
-                uint32_t r0[32], r1[32], qa[16], qb[16];
-                tmem_ld32(t_base + 64, r0);
-                tmem_ld32(t_base + 96, r1);
-                tmem_wait(r0);
-                reg_fence(r1);
+                reg_fence(r2);
+                reg_fence(r3);
                 // every accumulator read of this tile is complete
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-                store(n_half);
-                scale_chunk(r0, sb_s + 64, sa, qa);
-                scale_chunk(r1, sb_s + 96, sa, qb);
-                stage(qa, qb);
-                store(n_half + 64);
+                {
+                    uint32_t qa[16], qb[16];
+                    scale_chunk(r0, sb_s, sa, qa);
+                    scale_chunk(r1, sb_s + 32, sa, qb);
+                    stage(qa, qb);
+                    store(n_half);
+                }
+                {
+                    uint32_t qa[16], qb[16];
+                    scale_chunk(r2, sb_s + 64, sa, qa);
+                    scale_chunk(r3, sb_s + 96, sa, qb);
+                    stage(qa, qb);
+                    store(n_half + 64);
+                }
+                acc_phase ^= 1u;
             }
-            acc_phase ^= 1u;
-        }
-        // the staging boxes stay valid until the stores have finished
-        if (lane == 0) bulk_wait_all();
-        __syncwarp();
+            // the staging boxes stay valid until the stores have finished
+            if (lane == 0) bulk_wait_all();
+            __syncwarp();
     }
 
     tc_fence_before();
