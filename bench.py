@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--moe-row-align", type=int, default=256, choices=[128, 256],
+                    help="expert segment alignment of the MoE layout (256: one pair tile per slot)")
     return ap.parse_args()
 
 
@@ -455,7 +457,8 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
     ids = torch.from_numpy(m.topk_ids).to(dev)
     w1 = ops.quantize_experts(to_dev(m.w1))
     w2 = ops.quantize_experts(to_dev(m.w2))
-    cap = ops.nvfp4_moe_capacity(T, k, E, 128)
+    align = args.moe_row_align
+    cap = ops.nvfp4_moe_capacity(T, k, E, align)
     off = torch.empty(E + 1, dtype=torch.int32, device=dev)
     gather = torch.empty(cap, dtype=torch.int32, device=dev)
     dst = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -476,7 +479,7 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
         return torch.cuda.Event(enable_timing=True)
 
     stages = [
-        lambda: ops.nvfp4_moe_permute(ids, T, k, E, 128, off, gather, cap, dst, pws, pws_b, stream),
+        lambda: ops.nvfp4_moe_permute(ids, T, k, E, align, off, gather, cap, dst, pws, pws_b, stream),
         lambda: ops.nvfp4_quantize_per_token(x, T, H, H, gather, cap, ops.PER_TOKEN, a["q"], a["sf"],
                                              a["s"], stream=stream),
         lambda: ops.nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], cap, off, E, w1["q"], w1["sf"],
@@ -524,7 +527,7 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
         "workload": "qwen3_30b_a3b_moe_4096tok_128e_top8 (hidden 2048, expert ffn 768)",
         "ms_per_step": round(total, 5),
         "tflops": round(world * flop / (total * 1e-3) / 1e12, 2),
-        "padded_rows": used_rows, "routed_rows": routed,
+        "padded_rows": used_rows, "routed_rows": routed, "row_align": align,
         "kernels_ms": {"permute": round(seg[0], 5), "gather_quantize": round(seg[1], 5),
                        "grouped_fc1": round(seg[2], 5), "swiglu_quantize": round(seg[3], 5),
                        "grouped_fc2": round(seg[4], 5), "combine": round(seg[5], 5)},

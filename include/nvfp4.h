@@ -198,7 +198,8 @@ NVFP4_API size_t nvfp4_moe_permute_workspace_bytes(int64_t tokens, int32_t topk,
  *                  is recorded.
  *  tokens, topk    >= 0 and 1..64.
  *  num_experts     1..1024.
- *  row_align       >= 1; the grouped GEMM needs 128.
+ *  row_align       >= 1; the grouped GEMM needs a multiple of 128 (256
+ *                  balances its tiles best).
  *  expert_offsets  int32 [num_experts + 1] (output).
  *  gather_rows     int32 [capacity] (output): source token of each row, -1 for
  *                  padding and for rows past expert_offsets[num_experts].
@@ -294,6 +295,12 @@ NVFP4_API nvfp4_status nvfp4_gemm_ex(
  *  rows_capacity    rows of A and Y; expert_offsets[E] must be <= rows_capacity
  *                   and every expert_offsets[e] % 128 == 0 (else
  *                   NVFP4_ERR_DEVICE_INPUT is recorded and the tile is skipped).
+ *                   When every offset is a multiple of 256 (nvfp4_moe_permute
+ *                   with row_align 256) the kernel walks 256-row slots, each a
+ *                   full two-SM tile, which spreads the tiles evenly over the
+ *                   SM pairs; with 128-row alignment an expert with an odd
+ *                   number of 128-row tiles computes (and drops) 128 rows
+ *                   past its segment.
  *  expert_offsets   int32 [E + 1] (device), nondecreasing.
  *  E                1..1024.
  *  b_q              uint8 [E, N, K/2]: expert e's packed weights at b_q + e*N*K/2.

@@ -378,7 +378,7 @@ struct PairTile {
 // tiles ends in a tile whose odd CTA reads rows past the expert (its results
 // are computed with this expert's B and never stored).
 template <bool kGrouped>
-__device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int num_pm) {
+__device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int num_pm, int mrows) {
     PairTile tl;
     if (!kGrouped) {
         const int mt = t % num_pm;
@@ -392,7 +392,7 @@ __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int
         return tl;
     }
     const int nt = t % p.num_n_tiles;
-    const int64_t m0 = static_cast<int64_t>(t / p.num_n_tiles) * 128;
+    const int64_t m0 = static_cast<int64_t>(t / p.num_n_tiles) * mrows;
     // the last expert e with offsets[e] <= m0 (empty experts are passed over)
     int lo = 0, hi = p.E - 1;
     while (lo < hi) {
@@ -401,7 +401,7 @@ __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int
         else hi = mid - 1;
     }
     const int64_t e_begin = __ldg(p.offsets + lo);
-    tl.run = (((m0 - e_begin) >> 7) & 1) == 0;
+    tl.run = mrows == 256 || (((m0 - e_begin) >> 7) & 1) == 0;
     tl.m_base = m0;
     tl.n0 = static_cast<int64_t>(nt) * kBN;
     tl.b_row0 = static_cast<int64_t>(lo) * p.N + tl.n0;
@@ -473,14 +473,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t tmem = *tmem_holder;
     pdl_wait();             // the producers of the operands and offsets have completed
     int tiles = num_pm * p.num_n_tiles;
+    int mrows = 128;   // grouped: rows per slot of the padded layout
     if (kGrouped) {
+        // A layout whose expert segments are all 256-row aligned is walked in
+        // 256-row slots, every one a pair tile (the strided assignment then
+        // gives every pair the same number of tiles); otherwise in 128-row
+        // slots, a pair tile starting at every second one of an expert.
+        bool misaligned = false;
+        for (int e = threadIdx.x; e <= p.E; e += blockDim.x) misaligned |= (__ldg(p.offsets + e) & 255) != 0;
+        mrows = __syncthreads_or(misaligned) ? 128 : 256;
         // slots of the padded layout in use: it ends at offsets[E]
         int64_t used = __ldg(p.offsets + p.E);
         if (used > p.M || used < 0) {
             if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
             used = used < 0 ? 0 : p.M;
         }
-        tiles = static_cast<int>((used + 127) / 128) * p.num_n_tiles;
+        tiles = static_cast<int>((used + mrows - 1) / mrows) * p.num_n_tiles;
     }
 
     // Roles by warpgroup.  Each branch starts with its warpgroup's register
@@ -504,7 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
+                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm, mrows);
                 if (!tl.run) continue;
                 if (kGrouped && !side_b && rank == 0 && (__ldg(p.offsets + tl.expert) & 127) != 0)
                     record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
@@ -573,7 +581,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const uint64_t a_desc0 = sw128_desc(sA);
             const uint64_t b_desc0 = sw128_desc(sB);
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
+                if (!pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
@@ -630,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (!pair_tile_at<kGrouped>(p, t, num_pm).run) continue;
+                if (!pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
                     got = __all_sync(0xFFFFFFFFu, got);
@@ -688,7 +696,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const uint32_t acc_empty_leader = peer_addr(acc_empty, 0);
             uint32_t acc_phase = 0;
             for (int t = pair; t < tiles; t += npairs) {
-                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm);
+                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm, mrows);
                 if (!tl.run) continue;
                 // this CTA's 128 rows lie inside the tile's row range, or wholly past it
                 const bool write = tl.m_base + rank * 128 < tl.row_end;

@@ -189,11 +189,19 @@ __global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowJob job, S
             break;
         }
         parity ^= 1u << d;
-        if (pad_row) {
+        // A padding row gets zero scale words; a zero row of the output (no
+        // source row) quantizes, per token, to zero codes, zero scales and S = 0,
+        // written directly.
+        if (pad_row || (MODE == kPerToken && zero_row)) {
             __syncwarp();
             issue(r + cfg.depth * stride, d);
             d = (d + 1 == cfg.depth) ? 0 : d + 1;
-            if (MODE != kAmaxOnly) zero_sf_row(sec ? job.t1.sf : job.t0.sf, kgroups, lr, lane);
+            zero_sf_row(sec ? job.t1.sf : job.t0.sf, kgroups, lr, lane);
+            if (!pad_row) {
+                uint2* qrow = reinterpret_cast<uint2*>(sec ? job.t1.q : job.t0.q) + lr * nblocks;
+                for (int b = lane; b < nblocks; b += 32) qrow[b] = make_uint2(0u, 0u);
+                if (lane == 0) (sec ? job.t1.s : job.t0.s)[lr] = 0.0f;
+            }
             continue;
         }
         const uint4* row = reinterpret_cast<const uint4*>(bufs + static_cast<size_t>(d) * cfg.row_pad);

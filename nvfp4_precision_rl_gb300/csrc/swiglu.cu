@@ -53,21 +53,42 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(SwiParams p) {
             zero_sf_row(p.sf, p.kgroups, r, lane);
             continue;
         }
-        uint4 v[NCH];
+        uint4 g[NCH], u[NCH];
         const uint4* gr = reinterpret_cast<const uint4*>(p.y1 + r * p.ld);
         const uint4* ur = reinterpret_cast<const uint4*>(p.y1 + r * p.ld + p.ffn);
+        uint32_t bits = 0u;
 #pragma unroll
         for (int i = 0; i < NCH; ++i) {
             const int c = i * 32 + lane;
-            uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+            g[i] = make_uint4(0u, 0u, 0u, 0u);
+            u[i] = g[i];
             if (r < limit && c < nchunks) {
-                const uint4 g = ldg_stream(gr + c);
-                const uint4 u = ldg_stream(ur + c);
-                hv.x = swiglu_pair(g.x, u.x);
-                hv.y = swiglu_pair(g.y, u.y);
-                hv.z = swiglu_pair(g.z, u.z);
-                hv.w = swiglu_pair(g.w, u.w);
+                g[i] = ldg_stream(gr + c);
+                u[i] = ldg_stream(ur + c);
             }
+            bits |= g[i].x | g[i].y | g[i].z | g[i].w | u[i].x | u[i].y | u[i].z | u[i].w;
+        }
+        // A row whose inputs are all +0 (an expert layout's padding, or a row
+        // past row_count) gives h = +0 and quantizes to zero codes, zero
+        // scales and S = 0: written directly.
+        if (!__any_sync(0xFFFFFFFFu, bits != 0u)) {
+            for (int c = lane; c < nchunks; c += 32) {
+                p.q[r * nchunks + c] = 0u;
+                if (p.h != nullptr) reinterpret_cast<uint4*>(p.h + r * p.ffn)[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            zero_sf_row(p.sf, p.kgroups, r, lane);
+            if (lane == 0) p.s[r] = 0.0f;
+            continue;
+        }
+        uint4 v[NCH];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            const int c = i * 32 + lane;
+            uint4 hv;
+            hv.x = swiglu_pair(g[i].x, u[i].x);
+            hv.y = swiglu_pair(g[i].y, u[i].y);
+            hv.z = swiglu_pair(g[i].z, u[i].z);
+            hv.w = swiglu_pair(g[i].w, u[i].w);
             if (p.h != nullptr && c < nchunks)
                 reinterpret_cast<uint4*>(p.h + r * p.ffn)[c] = hv;
             v[i] = hv;

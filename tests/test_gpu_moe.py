@@ -80,17 +80,18 @@ def test_swiglu_row_count(nv):
     assert got["s"][:200].gt(0).all()
 
 
-def _grouped_case(nv, orc, T, H, N, E, k, seed, sample=None, experts_checked=None):
+def _grouped_case(nv, orc, T, H, N, E, k, seed, sample=None, experts_checked=None, align=128):
     x = W.small_matrix(seed, T, H)
     w = W.small_matrix(seed + 1, E * N, H, std=0.02).reshape(E, N, H)
     ids = _ids(seed + 2, T, E, k)
-    perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E)
+    perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E, row_align=align)
     a = nv.quantize(to_dev(x), gather=perm["gather"])
     wq = nv.quantize_experts(to_dev(w.reshape(E * N, H)).reshape(E, N, H))
     y = nv.grouped_gemm(a, perm["offsets"], E, wq["q"], wq["sf"], wq["s"], N, H)
     torch.cuda.synchronize()
     assert nv.nvfp4_get_device_status() == 0
-    rperm = orc.moe_permute(ids, E, 128, capacity=perm["capacity"])
+    rperm = orc.moe_permute(ids, E, align, capacity=perm["capacity"])
+    assert np.array_equal(perm["offsets"].cpu().numpy(), rperm["offsets"])
     off = rperm["offsets"]
     ra = orc.quantize(x, gather=rperm["gather"])
     yg = bf16_to_f64(y)
@@ -118,6 +119,17 @@ def _grouped_case(nv, orc, T, H, N, E, k, seed, sample=None, experts_checked=Non
                                        (500, 768, 272, 8, 2)])
 def test_grouped_gemm_small(nv, orc, T, H, N, E, k):
     _grouped_case(nv, orc, T, H, N, E, k, seed=T + N)
+
+
+@pytest.mark.parametrize("T,H,N,E,k", [(300, 256, 384, 16, 4), (40, 512, 256, 64, 2)])
+def test_grouped_gemm_256_aligned(nv, orc, T, H, N, E, k):
+    """Expert segments padded to 256 rows: the kernel walks 256-row slots."""
+    _grouped_case(nv, orc, T, H, N, E, k, seed=T + N + 7, align=256)
+
+
+def test_grouped_fc1_config3_sampled_256_aligned(nv, orc):
+    _grouped_case(nv, orc, 4096, 2048, 1536, 128, 8, seed=33, sample=300,
+                  experts_checked=[0, 2, 64, 127], align=256)
 
 
 def test_grouped_fc1_config3_sampled(nv, orc):
