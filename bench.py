@@ -304,7 +304,48 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step = max_over_ranks(float(np.mean(e2e_ms)), dev, world)
+    e2e_serial = max_over_ranks(float(np.mean(e2e_ms)), dev, world)
+
+    # the same, pipelined as a serving / training loop runs it: copy-in, compute
+    # and copy-out on three streams with double-buffered staging, so step i's
+    # output copy and step i+1's input copy overlap the compute; every step
+    # still moves its own X in and its own Y out inside the timed window
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    xs = [torch.empty_like(x) for _ in range(2)]
+    ys = [torch.empty_like(y) for _ in range(2)]
+    yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+
+    def pipe_step(i):
+        b = i % 2
+        if i >= 2:
+            s_in.wait_event(comp_done[b])          # xs[b] was read by step i-2
+        with torch.cuda.stream(s_in):
+            xs[b].copy_(x_host, non_blocking=True)
+        in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        if i >= 2:
+            stream.wait_event(out_done[b])         # ys[b] of step i-2 is on the host
+        quant_xw(xs[b])
+        ops.nvfp4_gemm(qx["q"], qx["sf"], qx["s"], M, qw["q"], qw["sf"], qw["s"], N, K, ys[b], N, stream)
+        comp_done[b].record(stream)
+        s_out.wait_event(comp_done[b])
+        with torch.cuda.stream(s_out):
+            yh[b].copy_(ys[b], non_blocking=True)
+        out_done[b].record(s_out)
+
+    for i in range(max(3, args.warmup)):
+        pipe_step(i)
+    torch.cuda.synchronize()
+    p0, p1 = ev(), ev()
+    p0.record(s_in)
+    for i in range(args.steps):
+        pipe_step(i + 2 * max(3, args.warmup))
+    p1.record(s_out)
+    torch.cuda.synchronize()
+    e2e_step = max_over_ranks(p0.elapsed_time(p1) / args.steps, dev, world)
     e2e_value = job_throughput(flop, world, e2e_step * 1e-3) / 1e12
 
     hbm_gbs, bf16_burst, bf16_sust, peak_src = measured_peaks()
@@ -330,7 +371,11 @@ def run_ours(args, rank, world, local_rank):
                    "launch": "the step (quantize + GEMM) captured once as one CUDA graph and replayed; kernels_ms from one graph per stage"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(M * K * 2), "d2h_bytes_per_step": int(M * N * 2),
-                "ms_per_step": round(e2e_step, 5)},
+                "ms_per_step": round(e2e_step, 5),
+                "mode": "pipelined: copy-in / compute / copy-out streams, double-buffered staging, "
+                        "no L2 flush (the step's working set exceeds L2)",
+                "serial_ms_per_step": round(e2e_serial, 5),
+                "serial_value": round(job_throughput(flop, world, e2e_serial * 1e-3) / 1e12, 2)},
         "roofline": {"kernel": "nvfp4_gemm_pair_kernel", "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp4_peak, 4),
