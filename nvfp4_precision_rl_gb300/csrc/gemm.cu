@@ -33,7 +33,7 @@
 //               accumulator, then scale by S_a * S_b with packed FP32x2
 //               multiplies, round to bf16, stage in 128-byte swizzled shared
 //               memory and store with TMA.  setmaxnreg moves registers from the
-//               producer / MMA and scale warpgroups (56 and 80 per thread) to
+//               producer / MMA and scale warpgroups (64 and 80 per thread) to
 //               the epilogue warpgroups (184), which hold the 128 columns.
 // Tile 256 x 256 per pair, K step of 256 FP4 = 128 bytes = one swizzle row.
 // The grouped (MoE) variant walks the padded per-expert layout (128-row
@@ -254,7 +254,7 @@ constexpr int kPThreads = 32 * (kFirstEpiWarp + kEpiWarps);       // 512
 // hold a whole 128-column half of the accumulator.  The sum must stay within
 // the launch's total, or setmaxnreg.inc would wait for registers forever.
 constexpr int kRegsLaunch = 128;
-constexpr int kRegsWG0 = 56;
+constexpr int kRegsWG0 = 64;
 constexpr int kRegsWG1 = 80;
 constexpr int kRegsEpi = 184;
 static_assert(kPThreads == 512, "four warpgroups");
