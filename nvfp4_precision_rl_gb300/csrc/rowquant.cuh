@@ -144,16 +144,9 @@ __device__ __forceinline__ void encode_row_blocks(const Block16 (&v)[NB], const 
         const float2 r2 = make_float2(rb, rb);
         const uint2 w = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
         if (b < nblocks) qrow[b] = w;
-        // four consecutive blocks = four consecutive lanes -> one scale word
-        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
-        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-        if ((lane & 3) == 0) {
-            const int g = b >> 2;
-            if (g < kgroups)
-                *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, g, kgroups)) =
-                    sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        }
+        // each lane writes its block's scale byte: four consecutive lanes fill
+        // one swizzled word (blocks past the row's end write zero bytes)
+        if ((b >> 2) < kgroups) sf[sf_word_offset(r, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
     }
     if (lane == 0) s[r] = rec.S;
 }
