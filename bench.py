@@ -392,58 +392,74 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 3 * args.steps,
         "wall_s_timed_loop": round(t_wall, 3),
     }
-    # NVFP4 -> bf16 dequantization of the same activation (the dequantized backward's input)
-    yx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-    dq = [lambda: ops.nvfp4_dequantize(qx["q"], qx["sf"], qx["s"], 1, M, K, yx, K, stream)]
-    for _ in range(3):
-        dq[0]()
-    torch.cuda.synchronize()
-    (gdq,) = capture_graphs(torch, dq, stream)
-    dq_ms = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e0, e1 = ev(), ev()
-        e0.record(stream)
-        gdq.replay()
-        e1.record(stream)
+    # Short kernels are timed ROT calls to a graph over ROT distinct buffer sets
+    # (together larger than L2), per-call average: one graph per call would add
+    # the graph launch (several microseconds) to every call.
+    ROT = 8
+
+    def time_rotating(fns):
+        for _ in range(2):
+            for fn in fns:
+                fn()
         torch.cuda.synchronize()
-        dq_ms.append(e0.elapsed_time(e1))
-    dq_t = float(np.mean(dq_ms))
-    dq_bytes = M * K * 0.5 + M * K / 16 + M * 4 + M * K * 2
-    result["dequantize"] = {"ms": round(dq_t, 5), "gbs": round(dq_bytes / (dq_t * 1e-3) / 1e9, 1),
-                            "frac_of_hbm": round(dq_bytes / (dq_t * 1e-3) / 1e9 / hbm_gbs, 4),
-                            "shape": [M, K]}
-    result["gpu_launches"] += args.steps
-    # MXFP8 of the same activation: 1x32 row copy + 32x1 column copy, then the
-    # row copy dequantized back to bf16
-    mx = ops.mxfp8_quantize(x, column_copy=True)
-    ymx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-    mxs = [lambda: ops.nvfp4_mxfp8_quantize(x, M, K, K, mx["q"], mx["sf"], mx["q_col"], mx["sf_col"], stream),
-           lambda: ops.nvfp4_mxfp8_dequantize(mx["q"], mx["sf"], M, K, ymx, K, stream)]
-    for _ in range(3):
-        for fn in mxs:
-            fn()
-    torch.cuda.synchronize()
-    gmx = capture_graphs(torch, mxs, stream)
-    mx_ms = [[], []]
-    for _ in range(args.steps):
-        for i, g in enumerate(gmx):
+        (g,) = capture_graphs(torch, [lambda: [fn() for fn in fns]], stream)
+        ts = []
+        for _ in range(args.steps):
             flush.zero_()
             e0, e1 = ev(), ev()
             e0.record(stream)
             g.replay()
             e1.record(stream)
             torch.cuda.synchronize()
-            mx_ms[i].append(e0.elapsed_time(e1))
-    t_mq, t_md = float(np.mean(mx_ms[0])), float(np.mean(mx_ms[1]))
+            ts.append(e0.elapsed_time(e1) / len(fns))
+        return float(np.mean(ts))
+
+    rot_note = f"{ROT} calls per graph over {ROT} buffer sets (> L2), per-call average"
+    # the step's quantize (X rows + column copy, W rows) per call, same method
+    q_sets = []
+    for _ in range(ROT):
+        xi, wi = x.clone(), w.clone()
+        q_sets.append(dict(x=xi, w=wi, qx=ops.quantize(xi, column_copy=True), qw=ops.quantize(wi)))
+
+    def q_call(c):
+        ops.nvfp4_quantize_per_token_pair(c["x"], M, K, c["qx"]["q"], c["qx"]["sf"], c["qx"]["s"], c["qx"]["q_col"],
+                                          c["qx"]["sf_col"], c["qx"]["s_col"], c["w"], N, K, c["qw"]["q"],
+                                          c["qw"]["sf"], c["qw"]["s"], K, wsbuf, wsb, stream)
+    t_qrot = time_rotating([lambda c=c: q_call(c) for c in q_sets])
+    result["quantize"]["per_call_ms"] = round(t_qrot, 5)
+    result["quantize"]["per_call_gbs"] = round((qx_bytes + qw_bytes) / (t_qrot * 1e-3) / 1e9, 1)
+    result["quantize"]["per_call_frac"] = round((qx_bytes + qw_bytes) / (t_qrot * 1e-3) / 1e9 / hbm_gbs, 4)
+    result["quantize"]["per_call_timing"] = rot_note
+    result["gpu_launches"] += 2 * ROT * args.steps
+    del q_sets
+    # NVFP4 -> bf16 dequantization of the same activation (the dequantized backward's input)
+    dq_src = [dict(q=qx["q"].clone(), sf=qx["sf"].clone(), s=qx["s"].clone()) for _ in range(ROT)]
+    dq_out = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(ROT)]
+    dq_t = time_rotating([lambda a=a, o=o: ops.nvfp4_dequantize(a["q"], a["sf"], a["s"], 1, M, K, o, K, stream)
+                          for a, o in zip(dq_src, dq_out)])
+    dq_bytes = M * K * 0.5 + M * K / 16 + M * 4 + M * K * 2
+    result["dequantize"] = {"ms": round(dq_t, 5), "gbs": round(dq_bytes / (dq_t * 1e-3) / 1e9, 1),
+                            "frac_of_hbm": round(dq_bytes / (dq_t * 1e-3) / 1e9 / hbm_gbs, 4),
+                            "shape": [M, K], "timing": rot_note}
+    result["gpu_launches"] += ROT * args.steps
+    # MXFP8 of the same activation: 1x32 row copy + 32x1 column copy, then the
+    # row copy dequantized back to bf16
+    mx_x = [x.clone() for _ in range(ROT)]
+    mx_out = [ops.mxfp8_quantize(xi, column_copy=True) for xi in mx_x]
+    t_mq = time_rotating([lambda xi=xi, o=o: ops.nvfp4_mxfp8_quantize(xi, M, K, K, o["q"], o["sf"], o["q_col"],
+                                                                      o["sf_col"], stream)
+                          for xi, o in zip(mx_x, mx_out)])
+    ymx = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(ROT)]
+    t_md = time_rotating([lambda o=o, yo=yo: ops.nvfp4_mxfp8_dequantize(o["q"], o["sf"], M, K, yo, K, stream)
+                          for o, yo in zip(mx_out, ymx)])
     mq_bytes = M * K * 2 + 2 * (M * K + M * K / 32)     # read X once; both copies written
     md_bytes = M * K + M * K / 32 + M * K * 2
     result["mxfp8"] = {"quantize_row_col_ms": round(t_mq, 5),
                        "quantize_gbs": round(mq_bytes / (t_mq * 1e-3) / 1e9, 1),
                        "dequantize_ms": round(t_md, 5),
                        "dequantize_gbs": round(md_bytes / (t_md * 1e-3) / 1e9, 1),
-                       "shape": [M, K]}
-    result["gpu_launches"] += 3 * args.steps
+                       "shape": [M, K], "timing": rot_note}
+    result["gpu_launches"] += 3 * ROT * args.steps
     # NVFP4 backward GEMMs on the same layer (column-wise copies, one scale each):
     # dgrad dX = dY W and wgrad dW = dY^T X; dY is a synthetic gradient [M, N]
     dy = to_dev(W.small_matrix(77, M, N, std=1e-3))
