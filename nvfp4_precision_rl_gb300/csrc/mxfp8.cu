@@ -193,15 +193,20 @@ nvfp4_status nvfp4_mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int
     if (!aligned(x, 16) || !aligned(q, 16) || !aligned(q_col, 16)) return NVFP4_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    // the padding of the swizzled scales reads as zero
-    if (cudaMemsetAsync(sf, 0, nvfp4_mxfp8_sf_bytes(rows, cols), s) != cudaSuccess) return NVFP4_ERR_CUDA;
     const int nb = static_cast<int>(cols / 32);
+    // the padding of the swizzled scales reads as zero (the kernels write every
+    // real block; there is padding only for ragged row or block counts)
+    if ((rows % 128 != 0 || nb % 4 != 0) &&
+        cudaMemsetAsync(sf, 0, nvfp4_mxfp8_sf_bytes(rows, cols), s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
     mx_rows_kernel<<<grid_for(rows * nb, ctx), kMxThreads, 0, s>>>(xb, rows, nb, ld_x, static_cast<uint8_t*>(q),
                                                                     static_cast<uint8_t*>(sf), (nb + 3) / 4);
     NVFP4_CHECK_LAUNCH();
     if (want_col) {
-        if (cudaMemsetAsync(sf_col, 0, nvfp4_mxfp8_sf_bytes(cols, rows), s) != cudaSuccess) return NVFP4_ERR_CUDA;
         const int nbc = static_cast<int>(rows / 32);
+        if ((cols % 128 != 0 || nbc % 4 != 0) &&
+            cudaMemsetAsync(sf_col, 0, nvfp4_mxfp8_sf_bytes(cols, rows), s) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
         mx_cols_kernel<<<grid_for((cols / 2) * nbc, ctx), kMxThreads, 0, s>>>(
             xb, rows, static_cast<int>(cols), ld_x, static_cast<uint8_t*>(q_col), static_cast<uint8_t*>(sf_col),
             (nbc + 3) / 4);
