@@ -525,6 +525,9 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
     dst = torch.empty((T, k), dtype=torch.int32, device=dev)
     pws_b = ops.nvfp4_moe_permute_workspace_bytes(T, k, E)
     pws = torch.empty(pws_b, dtype=torch.uint8, device=dev)
+    xq = dict(q=torch.empty((T, H // 2), dtype=torch.uint8, device=dev),
+              sf=torch.empty(ops.nvfp4_sf_bytes(T, H), dtype=torch.uint8, device=dev),
+              s=torch.empty(T, dtype=torch.float32, device=dev))
     a = dict(rows=cap, cols=H, q=torch.empty((cap, H // 2), dtype=torch.uint8, device=dev),
              sf=torch.empty(ops.nvfp4_sf_bytes(cap, H), dtype=torch.uint8, device=dev),
              s=torch.empty(cap, dtype=torch.float32, device=dev))
@@ -541,8 +544,12 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
 
     stages = [
         lambda: ops.nvfp4_moe_permute(ids, T, k, E, align, off, gather, cap, dst, pws, pws_b, stream),
-        lambda: ops.nvfp4_quantize_per_token(x, T, H, H, gather, cap, ops.PER_TOKEN, a["q"], a["sf"],
-                                             a["s"], stream=stream),
+        # per-token quantization of the tokens once, then their rows copied to the
+        # routed layout (equal, bit for bit, to quantizing the gathered rows)
+        lambda: ops.nvfp4_quantize_per_token(x, T, H, H, None, T, ops.PER_TOKEN, xq["q"], xq["sf"], xq["s"],
+                                             stream=stream),
+        lambda: ops.nvfp4_moe_gather_quantized(xq["q"], xq["sf"], xq["s"], T, H, gather, cap, a["q"], a["sf"],
+                                               a["s"], stream),
         lambda: ops.nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], cap, off, E, w1["q"], w1["sf"],
                                        w1["s"], 2 * F, H, y1, stream),
         lambda: ops.nvfp4_swiglu_quantize(y1, cap, F, 2 * F, off[E:], hq["q"], hq["sf"], hq["s"], None,
@@ -602,20 +609,21 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
         "launch": "the step captured as one CUDA graph; kernels_ms from one graph per stage",
         "tflops": round(world * flop / (total * 1e-3) / 1e12, 2),
         "padded_rows": used_rows, "routed_rows": routed, "row_align": align,
-        "kernels_ms": {"permute": round(seg[0], 5), "gather_quantize": round(seg[1], 5),
-                       "grouped_fc1": round(seg[2], 5), "swiglu_quantize": round(seg[3], 5),
-                       "grouped_fc2": round(seg[4], 5), "combine": round(seg[5], 5)},
+        "kernels_ms": {"permute": round(seg[0], 5), "quantize_tokens": round(seg[1], 5),
+                       "gather_quantized": round(seg[2], 5), "grouped_fc1": round(seg[3], 5),
+                       "swiglu_quantize": round(seg[4], 5), "grouped_fc2": round(seg[5], 5),
+                       "combine": round(seg[6], 5)},
         # combine: reads top-k rows of the fc2 output per token, writes one row
-        "combine_gbs": round((routed * H * 2 + T * H * 2 + routed * 8) / (seg[5] * 1e-3) / 1e9, 1),
-        "grouped_fc1": {"tflops": round(fc1_flop / (seg[2] * 1e-3) / 1e12, 1),
-                        "frac_of_fp4_peak": round(fc1_flop / (seg[2] * 1e-3) / 1e12 / fp4_peak, 4),
-                        "weight_gbs": round(w1_bytes / (seg[2] * 1e-3) / 1e9, 1),
-                        "weight_frac_of_hbm": round(w1_bytes / (seg[2] * 1e-3) / 1e9 / hbm_gbs, 4)},
-        "grouped_fc2": {"tflops": round(fc2_flop / (seg[4] * 1e-3) / 1e12, 1),
-                        "frac_of_fp4_peak": round(fc2_flop / (seg[4] * 1e-3) / 1e12 / fp4_peak, 4),
-                        "weight_gbs": round(w2_bytes / (seg[4] * 1e-3) / 1e9, 1),
-                        "weight_frac_of_hbm": round(w2_bytes / (seg[4] * 1e-3) / 1e9 / hbm_gbs, 4)},
-        "launches": 16 * args.steps,   # stage graphs + one-graph step, 8 kernels each
+        "combine_gbs": round((routed * H * 2 + T * H * 2 + routed * 8) / (seg[6] * 1e-3) / 1e9, 1),
+        "grouped_fc1": {"tflops": round(fc1_flop / (seg[3] * 1e-3) / 1e12, 1),
+                        "frac_of_fp4_peak": round(fc1_flop / (seg[3] * 1e-3) / 1e12 / fp4_peak, 4),
+                        "weight_gbs": round(w1_bytes / (seg[3] * 1e-3) / 1e9, 1),
+                        "weight_frac_of_hbm": round(w1_bytes / (seg[3] * 1e-3) / 1e9 / hbm_gbs, 4)},
+        "grouped_fc2": {"tflops": round(fc2_flop / (seg[5] * 1e-3) / 1e12, 1),
+                        "frac_of_fp4_peak": round(fc2_flop / (seg[5] * 1e-3) / 1e12 / fp4_peak, 4),
+                        "weight_gbs": round(w2_bytes / (seg[5] * 1e-3) / 1e9, 1),
+                        "weight_frac_of_hbm": round(w2_bytes / (seg[5] * 1e-3) / 1e9 / hbm_gbs, 4)},
+        "launches": 18 * args.steps,   # stage graphs + one-graph step, 9 kernels each
     }
 
 

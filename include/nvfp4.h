@@ -239,6 +239,31 @@ NVFP4_API nvfp4_status nvfp4_moe_permute_noalloc(
     int32_t row_align, int32_t* expert_offsets, int32_t* gather_rows, int64_t capacity,
     int32_t* dst_rows, nvfp4_stream_t stream);
 
+/*
+ * Scatter per-token quantized rows into the routed (expert) layout: output row
+ * r is row gather_rows[r] of the source quantization -- its packed codes, its
+ * swizzled block-scale words and its FP32 outer scale -- or a zero row (zero
+ * codes, zero scales, S = 0) when gather_rows[r] < 0.  Per-token quantization
+ * of a row depends on that row alone ("Towards Blackwell-Native 8-bit and
+ * 4-bit RL", "Online computation of the per-token scale"), so
+ * nvfp4_quantize_per_token(X) followed by this call produces, bit for bit,
+ * what nvfp4_quantize_per_token(X, gather_rows) produces, with 1/topk of the
+ * quantization work.
+ *
+ *  q_src, sf_src, s_src  a per-token quantization of X [rows_src, cols]
+ *               (nvfp4_quantize_per_token without gather): uint8 [rows_src,
+ *               cols/2], nvfp4_sf_bytes(rows_src, cols) bytes, float [rows_src].
+ *  cols         > 0, % 16 == 0.
+ *  gather_rows  int32 [rows_out] (device); an index >= rows_src makes a zero row
+ *               and records NVFP4_ERR_DEVICE_INPUT.
+ *  q, sf, s     uint8 [rows_out, cols/2], nvfp4_sf_bytes(rows_out, cols) bytes
+ *               (scale rows past rows_out written as 0), float [rows_out].
+ *  Pointers 16-byte aligned (s, s_src, gather_rows: 4).  rows_out == 0 is a no-op.
+ */
+NVFP4_API nvfp4_status nvfp4_moe_gather_quantized(
+    const void* q_src, const void* sf_src, const float* s_src, int64_t rows_src, int64_t cols,
+    const int32_t* gather_rows, int64_t rows_out, void* q, void* sf, float* s, nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Block-scaled W4A4 GEMMs                                                   */
 /* ------------------------------------------------------------------------- */

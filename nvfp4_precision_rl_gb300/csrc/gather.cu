@@ -1,0 +1,124 @@
+// gather.cu -- per-token quantized rows scattered into the expert layout.
+//
+// Per-token quantization of a row depends on that row alone (its own amax,
+// S = amax / 2688, its own block scales and codes: "Towards Blackwell-Native
+// 8-bit and 4-bit RL", "Online computation of the per-token scale"), so
+// quantizing the tokens once and copying row gather[r] of the result to row r
+// of the routed layout gives, bit for bit, what quantizing the gathered rows
+// gives -- with top-k routing, at 1/k of the quantization work.  A row with no
+// source (layout padding) becomes a zero row (zero codes, zero scales, S = 0:
+// the quantization of a zero row); the scale rows past rows_out up to a
+// multiple of 128 are zeroed, as the quantizer does.
+#include "common.cuh"
+#include "rowquant.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kGqThreads = 256;
+
+// One CTA per 128-row tile of the output (a tile of the swizzled scale layout):
+// the tile's source rows are read once into shared memory; the codes are
+// copied in 16- (or 8-) byte pieces, consecutive threads on consecutive pieces
+// of a row; each 512-byte scale atom (128 rows x one word) is written as 32
+// 16-byte lines, lane l gathering the words of rows l, l+32, l+64, l+96.
+template <bool kVec16>
+__global__ void __launch_bounds__(kGqThreads) gather_quantized_kernel(
+    const uint8_t* __restrict__ q_src, const uint8_t* __restrict__ sf_src, const float* __restrict__ s_src,
+    int64_t rows_src, const int32_t* __restrict__ gather, int64_t rows_out, int64_t tiles, int row_bytes,
+    int kgroups, uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s, unsigned* status) {
+    pdl_launch_dependents();    // a dependent waits for this grid's completion itself
+    __shared__ int64_t src_of[128];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    constexpr int kPiece = kVec16 ? 16 : 8;
+    const int pieces = row_bytes / kPiece;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t r0 = tile * 128;
+        __syncthreads();                    // the previous tile's src_of is no longer read
+        if (threadIdx.x < 128) {
+            const int64_t r = r0 + threadIdx.x;
+            int64_t src = -1;
+            if (r < rows_out) {
+                src = __ldg(gather + r);
+                if (src >= rows_src) {
+                    record_error(status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
+                    src = -1;
+                }
+                s[r] = src >= 0 ? __ldg(s_src + src) : 0.0f;
+            }
+            src_of[threadIdx.x] = src;
+        }
+        __syncthreads();
+        // codes of the tile's rows (rows past rows_out have none)
+        const int64_t rows_here = rows_out - r0 < 128 ? rows_out - r0 : 128;
+        const int64_t items = rows_here * pieces;
+        for (int64_t it = threadIdx.x; it < items; it += kGqThreads) {
+            const int rr = static_cast<int>(it / pieces);
+            const int pc = static_cast<int>(it - static_cast<int64_t>(rr) * pieces);
+            const int64_t src = src_of[rr];
+            if (kVec16) {
+                const uint4 v = src >= 0 ? __ldg(reinterpret_cast<const uint4*>(q_src + src * row_bytes) + pc)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                reinterpret_cast<uint4*>(q + (r0 + rr) * row_bytes)[pc] = v;
+            } else {
+                const uint2 v = src >= 0 ? __ldg(reinterpret_cast<const uint2*>(q_src + src * row_bytes) + pc)
+                                         : make_uint2(0u, 0u);
+                reinterpret_cast<uint2*>(q + (r0 + rr) * row_bytes)[pc] = v;
+            }
+        }
+        // scale atoms: warp w builds atoms g = w, w + 8, ...; lane l writes line l
+        for (int g = warp; g < kgroups; g += kGqThreads / 32) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                const int64_t src = src_of[lane + 32 * qd];
+                w4[qd] = src >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sf_src + sf_word_offset(src, g, kgroups)))
+                                  : 0u;
+            }
+            reinterpret_cast<uint4*>(sf + (tile * kgroups + g) * 512)[lane] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+    }
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" nvfp4_status nvfp4_moe_gather_quantized(const void* q_src, const void* sf_src, const float* s_src,
+                                                   int64_t rows_src, int64_t cols, const int32_t* gather_rows,
+                                                   int64_t rows_out, void* q, void* sf, float* s,
+                                                   nvfp4_stream_t stream) {
+    DeviceCtx ctx;
+    nvfp4_status st = device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
+    if (rows_src < 0 || rows_out < 0 || cols <= 0 || cols % 16 != 0 || cols > (int64_t(1) << 24))
+        return NVFP4_ERR_SHAPE;
+    if (rows_out == 0) return NVFP4_OK;
+    if (gather_rows == nullptr || q == nullptr || sf == nullptr || s == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (rows_src > 0 && (q_src == nullptr || sf_src == nullptr || s_src == nullptr)) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(q_src, 16) || !aligned(sf_src, 16) || !aligned(s_src, 4) || !aligned(gather_rows, 4) ||
+        !aligned(q, 16) || !aligned(sf, 16) || !aligned(s, 4))
+        return NVFP4_ERR_ALIGNMENT;
+    const int row_bytes = static_cast<int>(cols / 2);
+    const int kgroups = static_cast<int>(ceil_div(cols, 64));
+    const int64_t tiles = ceil_div(rows_out, 128);
+    const int64_t cap = static_cast<int64_t>(ctx.sm_count) * 8;
+    const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t* qs = static_cast<const uint8_t*>(q_src);
+    const uint8_t* ss = static_cast<const uint8_t*>(sf_src);
+    if (row_bytes % 16 == 0)
+        gather_quantized_kernel<true><<<grid, kGqThreads, 0, cs>>>(qs, ss, s_src, rows_src, gather_rows, rows_out,
+                                                                   tiles, row_bytes, kgroups,
+                                                                   static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf),
+                                                                   s, ctx.status);
+    else
+        gather_quantized_kernel<false><<<grid, kGqThreads, 0, cs>>>(qs, ss, s_src, rows_src, gather_rows, rows_out,
+                                                                    tiles, row_bytes, kgroups,
+                                                                    static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf),
+                                                                    s, ctx.status);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
+}

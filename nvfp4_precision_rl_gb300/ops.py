@@ -64,6 +64,7 @@ def lib():
         "nvfp4_quantize_per_token_pair": (st, [P, I64, I64, P, P, P, P, P, P, P, I64, I64, P, P, P, I64, P,
                                                SZ, P]),
         "nvfp4_moe_combine": (st, [P, I64, I64, P, P, I64, ctypes.c_int32, I64, P, I64, P]),
+        "nvfp4_moe_gather_quantized": (st, [P, P, P, I64, I64, P, I64, P, P, P, P]),
         "nvfp4_mxfp8_sf_bytes": (SZ, [I64, I64]),
         "nvfp4_mxfp8_quantize": (st, [P, I64, I64, I64, P, P, P, P, P]),
         "nvfp4_mxfp8_dequantize": (st, [P, P, I64, I64, P, I64, P]),
@@ -179,6 +180,13 @@ def nvfp4_gemm_ex(a_q, a_sf, a_s, a_s_per_row, M, b_q, b_sf, b_s, b_s_per_row, N
 def nvfp4_dequantize(q, sf, s, s_per_row, rows, cols, y, ld_y, stream=None):
     _ok("nvfp4_dequantize", lib().nvfp4_dequantize(
         _p(q), _p(sf), _p(s), int(s_per_row), rows, cols, _p(y), ld_y, _s(stream)))
+
+
+def nvfp4_moe_gather_quantized(q_src, sf_src, s_src, rows_src, cols, gather_rows, rows_out, q, sf, s,
+                               stream=None):
+    _ok("nvfp4_moe_gather_quantized", lib().nvfp4_moe_gather_quantized(
+        _p(q_src), _p(sf_src), _p(s_src), rows_src, cols, _p(gather_rows), rows_out, _p(q), _p(sf), _p(s),
+        _s(stream)))
 
 
 def nvfp4_mxfp8_sf_bytes(rows, cols):
@@ -402,6 +410,20 @@ def dequantize(qres, column=False, out=None, stream=None):
     y = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device)
     nvfp4_dequantize(q, sf, s, per_row, rows, cols, y, y.stride(0), stream)
     return y
+
+
+def moe_gather_quantized(qres, gather, stream=None):
+    """Rows of a per-token quantize() result scattered to the routed layout
+    (row r = source row gather[r], zero row where gather[r] < 0)."""
+    rows_out = gather.shape[0]
+    cols = qres["cols"]
+    dev = qres["q"].device
+    out = dict(rows=rows_out, cols=cols, q=_u8((rows_out, cols // 2), dev),
+               sf=_u8(nvfp4_sf_bytes(rows_out, cols), dev),
+               s=torch.empty(rows_out, dtype=torch.float32, device=dev))
+    nvfp4_moe_gather_quantized(qres["q"], qres["sf"], qres["s"], qres["rows"], cols, gather, rows_out, out["q"],
+                               out["sf"], out["s"], stream)
+    return out
 
 
 def mxfp8_quantize(x, column_copy=False, stream=None):

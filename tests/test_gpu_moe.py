@@ -51,6 +51,31 @@ def test_gather_quantize_bit_exact(nv, orc):
     assert_quant_equal(got, ref, what="gather-quantize")
 
 
+@pytest.mark.parametrize("T,H,E,k,align", [(300, 512, 16, 4, 128), (100, 272, 8, 2, 256),
+                                           (4096, 2048, 128, 8, 256)])
+def test_gather_quantized_bit_exact(nv, orc, T, H, E, k, align):
+    """Quantize the tokens once, then scatter the quantized rows to the routed
+    layout: equal, bit for bit, to quantizing the gathered rows."""
+    x = W.small_matrix(23 + T, T, H, dist="lognormal_rows")
+    ids = _ids(24 + T, T, E, k)
+    perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E, row_align=align)
+    rperm = orc.moe_permute(ids, E, align, capacity=perm["capacity"])
+    got = nv.moe_gather_quantized(nv.quantize(to_dev(x)), perm["gather"])
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_status() == 0
+    ref = orc.quantize(x, gather=rperm["gather"])
+    assert_quant_equal(got, ref, what="gather of quantized rows")
+
+
+def test_gather_quantized_bad_index(nv):
+    q = nv.quantize(torch.randn(8, 64, device="cuda").to(torch.bfloat16))
+    g = torch.tensor([0, 7, 8, -1], dtype=torch.int32, device="cuda")
+    out = nv.moe_gather_quantized(q, g)
+    assert nv.nvfp4_get_device_status() == 7          # NVFP4_ERR_DEVICE_INPUT
+    assert not out["q"][2:].any() and not out["s"][2:].any()
+    assert torch.equal(out["q"][1], q["q"][7]) and out["s"][1] == q["s"][7]
+
+
 @pytest.mark.parametrize("R,F", [(300, 768), (129, 64), (64, 2048)])
 def test_swiglu_quantize(nv, orc, R, F):
     rng = np.random.default_rng(R + F)
