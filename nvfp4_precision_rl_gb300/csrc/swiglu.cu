@@ -3,7 +3,8 @@
 // writing h to HBM unless asked ("Towards Blackwell-Native 8-bit and 4-bit RL",
 // "Parallelism and tensor-conversion contract": gate and up projections are one
 // fused GEMM in a SwiGLU MoE layer).  The quantize step is the row quantizer's
-// own code (rowquant.cuh), so it is bit-exact given h.
+// own code (rowquant.cuh), so it is bit-exact given h; h itself is within one
+// bf16 ulp of bf16(silu(g) u) evaluated exactly.
 #include "rowquant.cuh"
 
 namespace nvfp4 {
@@ -25,8 +26,12 @@ struct SwiParams {
     int kgroups;
 };
 
+// silu(g) u in binary32 with the fast exponential and divide (each within a
+// few float ulps, ~2^-20 relative in all): far inside half a bf16 ulp
+// (2^-9), so h = bf16(silu(g) u) is within one bf16 ulp of the exact value --
+// the same bound an exactly rounded exponential would give.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    const float sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+    const float sg = __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
     return __fmul_rn(sg, u);
 }
 
