@@ -393,19 +393,41 @@ __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int
     }
     const int nt = t % p.num_n_tiles;
     const int64_t m0 = static_cast<int64_t>(t / p.num_n_tiles) * mrows;
-    // the last expert e with offsets[e] <= m0 (empty experts are passed over)
-    int lo = 0, hi = p.E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<int64_t>(__ldg(p.offsets + mid)) <= m0) lo = mid;
-        else hi = mid - 1;
+    // The last expert e with offsets[e] <= m0 (empty experts are passed over),
+    // i.e. (the number of e < E with offsets[e] <= m0) - 1 for nondecreasing
+    // offsets, found in two rounds of independent loads -- the first entry of
+    // each block of 16 experts, then the block's entries -- rather than a
+    // binary search's chain of dependent loads (each an L2 round trip here).
+    const int nblk = (p.E + 15) >> 4;
+    int cnt = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 8) {
+        int v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = (b0 + j < nblk) ? __ldg(p.offsets + 16 * (b0 + j)) : INT_MAX;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cnt += static_cast<int64_t>(v[j]) <= m0;
     }
-    const int64_t e_begin = __ldg(p.offsets + lo);
+    const int base = (cnt > 0 ? cnt - 1 : 0) << 4;
+    int w[17];
+#pragma unroll
+    for (int j = 0; j < 17; ++j) w[j] = (base + j <= p.E) ? __ldg(p.offsets + base + j) : INT_MAX;
+    int c2 = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) c2 += (base + j < p.E && static_cast<int64_t>(w[j]) <= m0);
+    const int jj = c2 > 0 ? c2 - 1 : 0;
+    const int lo = base + jj;
+    int64_t e_begin = w[0], e_end = w[1];
+#pragma unroll
+    for (int j = 1; j < 16; ++j)
+        if (j == jj) {
+            e_begin = w[j];
+            e_end = w[j + 1];
+        }
     tl.run = mrows == 256 || (((m0 - e_begin) >> 7) & 1) == 0;
     tl.m_base = m0;
     tl.n0 = static_cast<int64_t>(nt) * kBN;
     tl.b_row0 = static_cast<int64_t>(lo) * p.N + tl.n0;
-    tl.row_end = __ldg(p.offsets + lo + 1);
+    tl.row_end = e_end;
     tl.expert = lo;
     return tl;
 }
@@ -581,7 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const uint64_t a_desc0 = sw128_desc(sA);
             const uint64_t b_desc0 = sw128_desc(sB);
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (!pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
+                if (mrows != 256 && !pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
@@ -638,7 +660,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (!pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
+                if (mrows != 256 && !pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
                     got = __all_sync(0xFFFFFFFFu, got);
