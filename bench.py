@@ -107,14 +107,17 @@ def gemm_traffic(kernel_sha):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("gemm_cu_sha256") != kernel_sha or d.get("workload") != WORKLOAD:
+    if d.get("gemm_cu_code_sha256") != kernel_sha or d.get("workload") != WORKLOAD:
         return None
     return d.get("dram_bytes_per_launch")
 
 
-def file_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def code_sha(path):
+    """sha256 of a source file's code: // comments, trailing blanks and blank
+    lines removed, so a comment edit does not orphan counters taken on it."""
+    with open(path) as f:
+        lines = [ln.split("//", 1)[0].rstrip() for ln in f.read().splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
 
 
 class Clocks:
@@ -357,7 +360,7 @@ def run_ours(args, rank, world, local_rank):
     qx_bytes = qx_bytes_row + M * K * 0.5 + M * K / 16 + 4
     qw_bytes = N * K * 2 + N * K * 0.5 + N * K / 16 + N * 4
     q_gbs = (qx_bytes + qw_bytes) / (t_q.mean() * 1e-3) / 1e9
-    sha = file_sha(os.path.join(ROOT, "nvfp4_precision_rl_gb300", "csrc", "gemm.cu"))
+    sha = code_sha(os.path.join(ROOT, "nvfp4_precision_rl_gb300", "csrc", "gemm.cu"))
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,

@@ -36,9 +36,11 @@
 //               producer / MMA and scale warpgroups (64 and 80 per thread) to
 //               the epilogue warpgroups (184), which hold the 128 columns.
 // Tile 256 x 256 per pair, K step of 256 FP4 = 128 bytes = one swizzle row.
-// The grouped (MoE) variant walks the padded per-expert layout (128-row
-// aligned segments, device-side offsets): a pair tile covers two 128-row tiles
-// of one expert.
+// The grouped (MoE) variant walks the padded per-expert layout (device-side
+// offsets): a pair tile covers 256 rows of one expert -- with 128-row aligned
+// segments it starts at every second 128-row tile of an expert (an odd tail
+// computes, and drops, 128 rows past the expert), with 256-row aligned
+// segments every 256-row slot is a pair tile.
 //
 // Every wait is bounded: a wait that runs out sets the status word and a shared
 // abort flag, every role leaves its loop, the producers wait (bounded) for their
@@ -521,11 +523,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         if ((warp == 0 || warp == kPBWarp) && lane < kPLoadLanes) {
             // ------------------------------ producers (both CTAs) ------------------
             // Warp 0 loads A and its scales, warp kPBWarp this CTA's 128 rows of B
-            // and the B scales; kPLoadLanes lanes of each split the rows.  TMA
-            // copies issued by one thread are processed one after another (about
-            // 27 bytes per SM clock for 16 KB tiles), so a stage fills at the rate
-            // of its issuing threads.  (Two warps with one lane each measured
-            // fastest: 64-row boxes from two lanes each were slower.)
+            // and the B scales; kPLoadLanes lanes of each split the rows.  (One
+            // lane per warp with 128-row boxes measured as fast as two or four
+            // lanes with smaller boxes, and simpler.)
             const bool side_b = warp == kPBWarp;
             const int sub = lane;                     // which kPBoxRows-row part
             const CUtensorMap* map = side_b ? &tma_b : &tma_a;
