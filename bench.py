@@ -620,6 +620,16 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
     # weight bytes each grouped GEMM must read at least once (codes + scales + row scales)
     w1_bytes = E * (2 * F) * (H // 2 + H // 16 + 4)
     w2_bytes = E * H * (F // 2 + F // 16 + 4)
+    # every byte a grouped GEMM must move at least once: its quantized input
+    # rows (the padded layout's used rows), the expert weights and its bf16 output
+    fc1_io = used_rows * (H // 2 + H // 16 + 4) + w1_bytes + used_rows * 2 * F * 2
+    fc2_io = used_rows * (F // 2 + F // 16 + 4) + w2_bytes + used_rows * H * 2
+    # SwiGLU-quantize: reads the used rows of Y1, writes codes, scales and S of
+    # every row of the capacity (rows past the used ones are written as zeros)
+    swi_io = used_rows * 2 * F * 2 + cap * (F // 2 + 4) + ops.nvfp4_sf_bytes(cap, F)
+
+    def gbs(nbytes, ms):
+        return round(nbytes / (ms * 1e-3) / 1e9, 1)
     return {
         "workload": "qwen3_30b_a3b_moe_4096tok_128e_top8 (hidden 2048, expert ffn 768)",
         "ms_per_step": round(total, 5),
@@ -635,12 +645,18 @@ def run_moe(args, ops, W, torch, dev, stream, flush, world, fp4_peak, hbm_gbs):
         "combine_gbs": round((routed * H * 2 + T * H * 2 + routed * 8) / (seg[6] * 1e-3) / 1e9, 1),
         "grouped_fc1": {"tflops": round(fc1_flop / (seg[3] * 1e-3) / 1e12, 1),
                         "frac_of_fp4_peak": round(fc1_flop / (seg[3] * 1e-3) / 1e12 / fp4_peak, 4),
-                        "weight_gbs": round(w1_bytes / (seg[3] * 1e-3) / 1e9, 1),
-                        "weight_frac_of_hbm": round(w1_bytes / (seg[3] * 1e-3) / 1e9 / hbm_gbs, 4)},
+                        "weight_gbs": gbs(w1_bytes, seg[3]),
+                        "weight_frac_of_hbm": round(gbs(w1_bytes, seg[3]) / hbm_gbs, 4),
+                        "io_bytes": int(fc1_io), "io_gbs": gbs(fc1_io, seg[3]),
+                        "io_frac_of_hbm": round(gbs(fc1_io, seg[3]) / hbm_gbs, 4)},
         "grouped_fc2": {"tflops": round(fc2_flop / (seg[5] * 1e-3) / 1e12, 1),
                         "frac_of_fp4_peak": round(fc2_flop / (seg[5] * 1e-3) / 1e12 / fp4_peak, 4),
-                        "weight_gbs": round(w2_bytes / (seg[5] * 1e-3) / 1e9, 1),
-                        "weight_frac_of_hbm": round(w2_bytes / (seg[5] * 1e-3) / 1e9 / hbm_gbs, 4)},
+                        "weight_gbs": gbs(w2_bytes, seg[5]),
+                        "weight_frac_of_hbm": round(gbs(w2_bytes, seg[5]) / hbm_gbs, 4),
+                        "io_bytes": int(fc2_io), "io_gbs": gbs(fc2_io, seg[5]),
+                        "io_frac_of_hbm": round(gbs(fc2_io, seg[5]) / hbm_gbs, 4)},
+        "swiglu_quantize": {"io_bytes": int(swi_io), "io_gbs": gbs(swi_io, seg[4]),
+                            "io_frac_of_hbm": round(gbs(swi_io, seg[4]) / hbm_gbs, 4)},
         "launches": 18 * args.steps,   # stage graphs + one-graph step, 9 kernels each
     }
 

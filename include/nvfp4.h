@@ -444,9 +444,11 @@ NVFP4_API nvfp4_status nvfp4_mxfp8_dequantize(
  * gate/up projection: "Towards Blackwell-Native 8-bit and 4-bit RL",
  * "Parallelism and tensor-conversion contract", SwiGLU MoE), then h quantized
  * per token exactly as nvfp4_quantize_per_token does, in the same kernel.
- * silu uses the fast exponential and divide (__expf, __fdividef: ~2^-20
- * relative error in binary32), so h may differ from an exact evaluation by one
- * bf16 ulp;
+ * silu is evaluated in binary32 with the hardware approximations ex2.approx
+ * and rcp.approx on exp(-|g|) (which never overflows: sigma(g) = 1/(1+e) for
+ * g >= 0, e/(1+e) for g < 0), ~2^-17 relative error at most, so h may differ
+ * from an exact evaluation by one bf16 ulp (for gates g >= -96; below that
+ * |silu(g)| < 1e-39 and the bound can fail when |u| is very large);
  * the quantization of h is bit-exact.
  *
  *  y1        bf16 [rows, ld_y1], ld_y1 >= 2*ffn, ld_y1 % 8 == 0, 16-byte aligned.

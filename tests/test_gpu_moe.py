@@ -76,7 +76,7 @@ def test_gather_quantized_bad_index(nv):
     assert torch.equal(out["q"][1], q["q"][7]) and out["s"][1] == q["s"][7]
 
 
-@pytest.mark.parametrize("R,F", [(300, 768), (129, 64), (64, 2048)])
+@pytest.mark.parametrize("R,F", [(300, 768), (77, 768), (200, 640), (129, 64), (64, 2048)])
 def test_swiglu_quantize(nv, orc, R, F):
     rng = np.random.default_rng(R + F)
     y1 = W.to_bf16_bits((rng.standard_normal((R, 2 * F)) * 2).astype(np.float32))
@@ -94,6 +94,25 @@ def test_swiglu_quantize(nv, orc, R, F):
     again = nv.quantize(got["h"])
     assert torch.equal(again["q"], got["q"]) and torch.equal(again["sf"], got["sf"])
     assert torch.equal(again["s"], got["s"])
+
+
+def test_swiglu_gate_tails(nv, orc):
+    """h within one bf16 ulp of the exact bf16(silu(g) u) across the gate's
+    range, including large negative gates where exp(-g) would overflow and
+    silu(g) is far below 1 (scaled up by large up-projection values)."""
+    F = 256
+    g = np.concatenate([np.linspace(-90.0, -20.0, 96), np.linspace(-20.0, 20.0, 128),
+                        np.linspace(20.0, 90.0, 32)]).astype(np.float32)
+    us = np.array([1.0, -1.0, 3.5, -300.0, 1.0e4, -1.0e4, 2.0 ** -60, 6.0e30], np.float32)
+    y1 = np.zeros((us.size, 2 * F), np.float32)
+    y1[:, :F] = g
+    y1[:, F:] = us[:, None]
+    bits = W.to_bf16_bits(y1)
+    got = nv.swiglu_quantize(to_dev(bits), F, want_h=True)
+    hg = bf16_to_f64(got["h"])
+    hr = W.bf16_bits_to_float(orc.swiglu(bits, F)).astype(np.float64)
+    bad = np.abs(hg - hr) > bf16_ulp(hr)
+    assert not bad.any(), f"{bad.sum()} values off by more than one bf16 ulp, e.g. g={np.nonzero(bad)}"
 
 
 def test_swiglu_row_count(nv):
