@@ -62,9 +62,11 @@ constexpr int kSFWarps = 4;                  // one per TMEM lane quadrant
 constexpr int kEpiWarps = 8;                 // two per TMEM lane quadrant, 128 columns each
 // Warp roles, aligned to warpgroups (setmaxnreg acts per warpgroup):
 //   warpgroup 0: warp 0 A producer, warp 1 TMEM allocation + MMA issuer (even
-//                CTA), warp 2 B producer, warp 3 idle;
+//                CTA), warp 2 B producer, warp 3 the grouped epilogue's tile
+//                scheduler (idle in the dense GEMM);
 //   warpgroup 1: warps 4..7 scale warps; warpgroups 2 and 3: epilogue.
 constexpr int kPBWarp = 2;                   // the B-side producer
+constexpr int kSchedWarp = 3;                // the epilogue's tile scheduler
 constexpr int kFirstSFWarp = 4;
 constexpr int kFirstEpiWarp = kFirstSFWarp + kSFWarps;
 constexpr uint32_t kATileBytes = kBM * kBKBytes;      // 16 KB
@@ -74,7 +76,23 @@ constexpr uint32_t kSFBTileBytes = 8 * kSFAtomBytes;  // 4 KB per stage
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSFTmemCol = 256;                  // after the 256 accumulator columns
 constexpr uint32_t kSFTmemPerStage = 48;              // 16 (A) + 32 (B)
-constexpr uint32_t kSBBytes = kEpiWarps * (kBN / 2) * 4; // per-warp copy of the tile's S_b half
+// Grouped GEMM: tile information for the epilogue, prepared one tile ahead by
+// the scheduler warp: the tile's origin, whether this CTA stores, this CTA's
+// 128 row scales S_a and the tile's 256 column scales S_b.  (The dense
+// epilogue finds its tile arithmetically and loads its scales itself, into a
+// per-warp copy of its S_b half in the same space.)
+struct EpiInfo {
+    int64_t m_base;
+    int64_t n0;
+    int32_t write;
+    int32_t end;       // 1: no more tiles for this pair
+    int32_t pad[2];
+    float sa[128];
+    float sb[kBN];
+};
+constexpr int kInfoSlots = 2;
+constexpr uint32_t kSBBytes = kInfoSlots * sizeof(EpiInfo) > kEpiWarps * (kBN / 2) * 4
+                                  ? kInfoSlots * sizeof(EpiInfo) : kEpiWarps * (kBN / 2) * 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;      // 0.2 s
 
@@ -452,14 +470,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     uint8_t* sSFA = sB + kPStages * kPBHalfBytes;
     uint8_t* sSFB = sSFA + kPStages * kSFATileBytes;
     uint8_t* sOut = sSFB + kPStages * kSFBTileBytes;              // 1024-aligned
-    float* sSB = reinterpret_cast<float*>(sOut + kPOutBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sSB) + kSBBytes);
+    EpiInfo* info = reinterpret_cast<EpiInfo*>(sOut + kPOutBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(info) + kSBBytes);
     uint64_t* empty = full + kPStages;
     uint64_t* sf_ready = empty + kPStages;
     uint64_t* acc_full = sf_ready + kPStages;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* drain = acc_empty + 1;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* info_full = drain + 1;            // [kInfoSlots]
+    uint64_t* info_empty = info_full + kInfoSlots;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(info_empty + kInfoSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -481,6 +501,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 2 * kEpiWarps);     // one arrival per epilogue warp of either CTA
         mbar_init(drain, 1);
+        for (int s = 0; s < kInfoSlots; ++s) {
+            mbar_init(&info_full[s], 1);          // the scheduler warp
+            mbar_init(&info_empty[s], kEpiWarps);  // this CTA's epilogue warps
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -651,6 +675,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             __syncwarp();
             if (!mbar_wait_bounded(drain, 0u, kDrainLimitNs, nullptr) && lane == 0)
                 record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_DRAIN);
+        } else if (kGrouped && warp == kSchedWarp) {
+            // ------------------------------ tile scheduler (both CTAs) -------------
+            // For each tile of this pair, in order: the tile lookup (for grouped
+            // layouts an expert search over the offsets, each load an L2 round
+            // trip) and the loads of the tile's S_a rows and S_b columns, written
+            // to the epilogue's ring one tile ahead, so that none of these
+            // latencies sits between two tiles of the epilogue.
+            uint32_t slot = 0, phase = 0;
+            bool ok = true;
+            for (int t = pair; t < tiles && ok; t += npairs) {
+                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm, mrows);
+                if (!tl.run) continue;
+                const int64_t mrow0 = tl.m_base + rank * 128;
+                float a[128 / 32], b[kBN / 32];
+    #pragma unroll
+                for (int i = 0; i < 128 / 32; ++i) {
+                    const int64_t m = mrow0 + i * 32 + lane;
+                    a[i] = (m < p.M) ? __ldg(p.sa + m * p.sa_stride) : 0.0f;
+                }
+                const float* sbp =
+                    p.sb + p.sb_stride * ((kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + tl.n0);
+    #pragma unroll
+                for (int i = 0; i < kBN / 32; ++i) {
+                    const int64_t n = tl.n0 + i * 32 + lane;
+                    b[i] = (n < p.N) ? __ldg(sbp + (i * 32 + lane) * p.sb_stride) : 0.0f;
+                }
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&info_empty[slot], phase ^ 1u, kWaitLimitNs, abort_flag));
+                if (!ok) break;
+                EpiInfo* e = info + slot;
+    #pragma unroll
+                for (int i = 0; i < 128 / 32; ++i) e->sa[i * 32 + lane] = a[i];
+    #pragma unroll
+                for (int i = 0; i < kBN / 32; ++i) e->sb[i * 32 + lane] = b[i];
+                if (lane == 0) {
+                    e->m_base = tl.m_base;
+                    e->n0 = tl.n0;
+                    // this CTA's 128 rows lie inside the tile's row range, or wholly past it
+                    e->write = mrow0 < tl.row_end;
+                    e->end = 0;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&info_full[slot]);
+                if (++slot == kInfoSlots) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok) {
+                // the end marker, once its slot is free
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&info_empty[slot], phase ^ 1u, kWaitLimitNs, abort_flag));
+                if (ok && lane == 0) {
+                    info[slot].end = 1;
+                    mbar_arrive(&info_full[slot]);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_EPILOGUE);
+            }
         }
     } else if (warp < kFirstEpiWarp) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG1));
@@ -712,29 +795,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const int ew = warp - kFirstEpiWarp;
             const int half = ew >> 2;
             const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
-            float* sb_s = sSB + ew * (kBN / 2);
             uint8_t* box = sOut + ew * kPOutBoxBytes;
             uint8_t* my_row = box + lane * 128;
             const uint32_t acc_empty_leader = peer_addr(acc_empty, 0);
-            uint32_t acc_phase = 0;
-            for (int t = pair; t < tiles; t += npairs) {
-                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm, mrows);
-                if (!tl.run) continue;
-                // this CTA's 128 rows lie inside the tile's row range, or wholly past it
-                const bool write = tl.m_base + rank * 128 < tl.row_end;
-                const int64_t row0 = tl.m_base + rank * 128 + quad * 32;
-                const int64_t m = row0 + lane;
-                const float sa = (m < p.M) ? __ldg(p.sa + m * p.sa_stride) : 0.0f;
-                const int64_t n_half = tl.n0 + half * (kBN / 2);
-                const float* sbp =
-                    p.sb + p.sb_stride * ((kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + n_half);
-                __syncwarp();
+            float* sb_w = reinterpret_cast<float*>(info) + ew * (kBN / 2);   // dense: this warp's S_b half
+            uint32_t acc_phase = 0, islot = 0, iphase = 0;
+            int t = pair;
+            for (;;) {
+                bool write;
+                int64_t row0, n_half;
+                float sa;
+                const float* sb_s;
+                if constexpr (kGrouped) {
+                    // the next tile's origin and scales, from the scheduler warp
+                    bool got = mbar_wait_bounded(&info_full[islot], iphase, kWaitLimitNs, abort_flag);
+                    got = __all_sync(0xFFFFFFFFu, got);
+                    if (!got) {
+                        *abort_flag = 1;
+                        if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_EPILOGUE);
+                        break;
+                    }
+                    const EpiInfo* ti = info + islot;
+                    if (ti->end) break;
+                    write = ti->write != 0;
+                    row0 = ti->m_base + rank * 128 + quad * 32;
+                    sa = ti->sa[quad * 32 + lane];
+                    n_half = ti->n0 + half * (kBN / 2);
+                    sb_s = ti->sb + half * (kBN / 2);
+                } else {
+                    if (t >= tiles) break;
+                    const PairTile tl = pair_tile_at<false>(p, t, num_pm, mrows);
+                    t += npairs;
+                    // this CTA's 128 rows lie inside the tile's row range, or wholly past it
+                    write = tl.m_base + rank * 128 < tl.row_end;
+                    row0 = tl.m_base + rank * 128 + quad * 32;
+                    const int64_t m = row0 + lane;
+                    sa = (m < p.M) ? __ldg(p.sa + m * p.sa_stride) : 0.0f;
+                    n_half = tl.n0 + half * (kBN / 2);
+                    const float* sbp = p.sb + p.sb_stride * n_half;
+                    __syncwarp();
     #pragma unroll
-                for (int i = 0; i < kBN / 2 / 32; ++i) {
-                    const int64_t n = n_half + i * 32 + lane;
-                    sb_s[i * 32 + lane] = (n < p.N) ? __ldg(sbp + (i * 32 + lane) * p.sb_stride) : 0.0f;
+                    for (int i = 0; i < kBN / 2 / 32; ++i) {
+                        const int64_t n = n_half + i * 32 + lane;
+                        sb_w[i * 32 + lane] = (n < p.N) ? __ldg(sbp + (i * 32 + lane) * p.sb_stride) : 0.0f;
+                    }
+                    __syncwarp();
+                    sb_s = sb_w;
                 }
-                __syncwarp();
                 bool ok = mbar_wait_cluster(acc_full, acc_phase, kWaitLimitNs, abort_flag);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) {
@@ -794,10 +901,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     uint32_t qa[16], qb[16];
                     scale_chunk(r2, sb_s + 64, sa, qa);
                     scale_chunk(r3, sb_s + 96, sa, qb);
+                    if constexpr (kGrouped) {
+                        // every read of this tile's ring slot is done
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&info_empty[islot]);
+                    }
                     stage(qa, qb);
                     store(n_half + 64);
                 }
                 acc_phase ^= 1u;
+                if (kGrouped && ++islot == kInfoSlots) {
+                    islot = 0;
+                    iphase ^= 1u;
+                }
             }
             // the staging boxes stay valid until the stores have finished
             if (lane == 0) bulk_wait_all();
