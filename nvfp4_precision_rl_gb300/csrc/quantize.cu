@@ -337,7 +337,6 @@ __device__ __forceinline__ uint2 encode_col_block(const uint32_t* v, float r) {
 // as two 16-byte stores when the row pitch allows it.
 template <bool kGather>
 __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
-    pdl_wait();                 // the row pass's amax (and any producer of x / gather)
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -346,9 +345,12 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
     if (g >= p.kgroups) return;
     const int64_t m0 = static_cast<int64_t>(g) * 64;
     const bool col_ok = k0 < p.cols;
-    const ScaleRecipe rec(__uint_as_float(*p.amax_ws));
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.s[0] = rec.S;
 
+    // x and the gather rows are complete before this kernel starts: the row
+    // pass it follows is launched without programmatic serialization, so it
+    // began only after their producers had finished, and this kernel begins
+    // after the row pass has.  The loads therefore run ahead of the wait;
+    // only the tensor amax comes from the row pass.
     uint32_t v[64];
     if (!kGather && col_ok && m0 + 64 <= p.rows_out) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(p.x + m0 * p.ld_x + k0);
@@ -369,6 +371,9 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(ColParams p) {
                        : 0u;
         }
     }
+    pdl_wait();                 // the row pass's tensor amax
+    const ScaleRecipe rec(__uint_as_float(*p.amax_ws));
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) p.s[0] = rec.S;
     uint32_t word0 = 0u, word1 = 0u;
     uint2 c0[4], c1[4];
 #pragma unroll
