@@ -584,7 +584,9 @@ nvfp4_status quantize_cols_launch(const uint16_t* x, int64_t rows_in, int64_t co
     dim3 grid(static_cast<unsigned>(round_up(cols, 128) / 64),
               static_cast<unsigned>(ceil_div(p.kgroups, kColThreads / 32)));
     // programmatic serialization: the kernel may start while the row pass
-    // finishes; it waits (griddepcontrol.wait) before reading anything
+    // finishes; it loads x at once and waits (griddepcontrol.wait) before
+    // reading the row pass's amax.  The row pass must therefore be launched
+    // without that attribute (it starts after x's producers have finished).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kColThreads, 1, 1);
