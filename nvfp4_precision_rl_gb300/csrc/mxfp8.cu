@@ -126,24 +126,29 @@ __global__ void __launch_bounds__(kMxThreads) mx_cols_kernel(const uint16_t* __r
 
 // Dequantization: one thread per block; dec(q) * 2^(code - 127) is exact in
 // binary32 and rounded once to bf16.
+// One thread per quarter block (8 values, 16 bytes of output): a warp's store
+// covers 512 contiguous bytes of a row.
 __global__ void __launch_bounds__(kMxThreads) mx_dequant_kernel(const uint8_t* __restrict__ q,
                                                                 const uint8_t* __restrict__ sf, int64_t rows,
                                                                 int nb, int kgroups, uint16_t* __restrict__ y,
                                                                 int64_t ld_y) {
-    const int64_t total = rows * nb;
+    const int parts = 4 * nb;                            // 8-value parts per row
+    const int64_t total = rows * parts;
+    const bool narrow = total <= 0xFFFFFFFFll;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t r = i / nb;
-        const int b = static_cast<int>(i - r * nb);
-        const uint4* src = reinterpret_cast<const uint4*>(q + r * (static_cast<int64_t>(nb) * 32) + b * 32);
-        const uint4 c0 = __ldg(src), c1 = __ldg(src + 1);
+        const int64_t r = narrow ? static_cast<int64_t>(static_cast<uint32_t>(i) / static_cast<uint32_t>(parts))
+                                 : i / parts;
+        const int pq = static_cast<int>(i - r * parts);
+        const int b = pq >> 2;
+        const uint2 c = __ldg(reinterpret_cast<const uint2*>(q + r * (static_cast<int64_t>(nb) * 32)) + pq);
         const uint32_t code = __ldg(sf + sf_word_offset(r, b >> 2, kgroups) + (b & 3));
         const float f = code ? __uint_as_float(code << 23) : __uint_as_float(0x00400000u);   // 2^(code-127)
         const float2 f2 = make_float2(f, f);
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t out[16];
+        const uint32_t words[2] = {c.x, c.y};
+        uint32_t out[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 2; ++j) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t hv;
@@ -154,9 +159,7 @@ __global__ void __launch_bounds__(kMxThreads) mx_dequant_kernel(const uint8_t* _
                 out[2 * j + h] = *reinterpret_cast<const uint32_t*>(&o);
             }
         }
-        uint4* dst = reinterpret_cast<uint4*>(y + r * ld_y + static_cast<int64_t>(b) * 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+        *reinterpret_cast<uint4*>(y + r * ld_y + static_cast<int64_t>(pq) * 8) = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
@@ -226,7 +229,7 @@ nvfp4_status nvfp4_mxfp8_dequantize(const void* q, const void* sf, int64_t rows,
     if (!q || !sf || !y) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(y, 16)) return NVFP4_ERR_ALIGNMENT;
     const int nb = static_cast<int>(cols / 32);
-    mx_dequant_kernel<<<grid_for(rows * nb, ctx), kMxThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+    mx_dequant_kernel<<<grid_for(rows * nb * 4, ctx), kMxThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint8_t*>(q), static_cast<const uint8_t*>(sf), rows, nb, (nb + 3) / 4,
         static_cast<uint16_t*>(y), ld_y);
     NVFP4_CHECK_LAUNCH();
