@@ -267,6 +267,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 //   scale warps (both CTAs) -> sf_ready of the even CTA (remote mbarrier arrive),
 //   MMA commits            -> empty / acc_full of both CTAs (multicast commit),
 //   epilogue (both CTAs)   -> acc_empty of the even CTA (remote arrive).
+// Within each CTA of the grouped kernel the scheduler warp and the epilogue
+// warps hand the tile-information ring back and forth through info_full /
+// info_empty (local arrivals).
 constexpr int kPStages = 5;
 constexpr int kPThreads = 32 * (kFirstEpiWarp + kEpiWarps);       // 512
 // Registers per thread after the split: the CTA launches with 128 per thread
