@@ -7,7 +7,9 @@ of 128 rows.  Pinned against numpy's stable argsort and invariants.
 
 SwiGLU: silu(gate) * up between the MoE fc1 and fc2 ("Towards Blackwell-Native
 8-bit and 4-bit RL", "Parallelism and tensor-conversion contract": gate and up
-projections fused into one GEMM).  Pinned against float64 numpy on exact inputs.
+projections fused into one GEMM).  Pinned against float64 numpy on exact inputs
+and, at chosen points across the gate's range, against 60-digit decimal
+arithmetic rounded to bfloat16 on integers.
 """
 import numpy as np
 
@@ -86,3 +88,57 @@ def test_swiglu_vs_float64(orc):
     # bf16 nearest: within half a bf16 ulp of the float64 value
     ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-38))) - 7)
     assert np.all(np.abs(hf - ref) <= ulp / 2 * (1 + 1e-12))
+
+
+def _bf16_nearest_bits(v):
+    """Bits of the bfloat16 nearest to the real number v (a Decimal), ties to
+    even, computed on integers: v = m 2^e with m in [2^7, 2^8) for normals."""
+    from decimal import Decimal
+    if v == 0:
+        return 0x8000 if v.is_signed() else 0
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    e = 0
+    while a >= 2:
+        a /= 2
+        e += 1
+    while a < 1:
+        a *= 2
+        e -= 1
+    # a in [1, 2): value = a 2^e; subnormals (e < -126) keep fewer bits
+    frac_bits = 7 if e >= -126 else 7 - (-126 - e)
+    scaled = a * (Decimal(2) ** frac_bits)
+    q = int(scaled)
+    rem = scaled - q
+    if rem > Decimal("0.5") or (rem == Decimal("0.5") and q % 2 == 1):
+        q += 1
+    if e >= -126:
+        if q == 256:                       # rounded up to the next binade
+            q, e = 128, e + 1
+        assert e <= 127, "overflow is not exercised here"
+        return sign | ((e + 127) << 7) | (q - 128)
+    return sign | q                        # subnormal: exponent field 0
+
+
+def test_swiglu_high_precision_points(orc):
+    """The oracle's h against silu(g) u evaluated with 60-digit decimal
+    arithmetic (its own exp) and rounded to bfloat16 on integers, across the
+    gate's range: exp(-g) near overflow, silu(g) far below 1, large and small
+    up-projection values."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 60
+    gates = [-90.0, -88.5, -50.0, -20.0, -3.5, -1.0, -0.125, 0.0, 0.125, 1.0, 3.5, 20.0, 90.0]
+    ups = [1.0, -3.0, 1000.0, 2.0 ** -60]
+    F = len(gates)
+    y1 = np.zeros((len(ups), 2 * F), np.float32)
+    y1[:, :F] = gates
+    y1[:, F:] = np.array(ups, np.float32)[:, None]
+    bits = W.to_bf16_bits(y1)
+    assert np.array_equal(W.bf16_bits_to_float(bits), y1), "test points must be bfloat16 values"
+    h = orc.swiglu(bits, F)
+    for i, u in enumerate(ups):
+        for j, g in enumerate(gates):
+            gd, ud = Decimal(g), Decimal(u)
+            exact = gd / (1 + (-gd).exp()) * ud
+            want = _bf16_nearest_bits(exact)
+            assert int(h[i, j]) == want, (g, u, hex(int(h[i, j])), hex(want))
