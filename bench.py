@@ -91,12 +91,19 @@ def capture_graphs(torch, stages, stream):
 
 
 def measured_peaks():
+    """HBM GB/s, bf16 burst and sustained TFLOP/s: the measured file's figures,
+    else (file or key missing, or unreadable) the fallback measurement."""
+    fallback = (6800.0, 1900.0, 1700.0)
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
+    try:
         with open(path) as f:
             d = json.load(f)
-        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
-    return 6800.0, 1900.0, 1700.0, "fallback"
+        vals = (d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"))
+    except (OSError, ValueError):
+        return fallback + ("fallback",)
+    if all(isinstance(v, (int, float)) and v > 0 for v in vals):
+        return vals + ("measured",)
+    return fallback + ("fallback",)
 
 
 def gemm_traffic(kernel_sha):
