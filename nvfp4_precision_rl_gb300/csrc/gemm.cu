@@ -115,6 +115,7 @@ struct GemmParams {
     int E;                    // grouped: experts; dense: 0
     int sa_stride;            // 1: S_a per row of A; 0: one S_a for all rows
     int sb_stride;            // 1: S_b per row of B; 0: one S_b for all rows
+    int n_fast;               // dense: 1 walks the tiles n-tile fastest, 0 m-tile fastest
 };
 
 // ----------------------------------------------------------------------------
@@ -395,7 +396,11 @@ struct PairTile {
     int expert;
 };
 
-// Dense: t -> (m-tile, n-tile), m fastest.  Grouped: t -> (128-row tile g of
+// Dense: t -> (m-tile, n-tile), the smaller operand's tile index fastest, so
+// the pairs working at one time share the larger operand's rows and that
+// operand streams from HBM once while the smaller one stays in L2 (with m
+// fastest at M = 65,536, N = 6,144 every n-tile would sweep all 67 MB of A
+// again while the bf16 output pushes it out of L2).  Grouped: t -> (128-row tile g of
 // the padded layout, n-tile), n fastest; a pair tile starts at every second
 // 128-row tile of an expert's segment, so an expert with an odd number of
 // tiles ends in a tile whose odd CTA reads rows past the expert (its results
@@ -404,8 +409,8 @@ template <bool kGrouped>
 __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int num_pm, int mrows) {
     PairTile tl;
     if (!kGrouped) {
-        const int mt = t % num_pm;
-        const int nt = t / num_pm;
+        const int mt = p.n_fast ? t / p.num_n_tiles : t % num_pm;
+        const int nt = p.n_fast ? t % p.num_n_tiles : t / num_pm;
         tl.run = true;
         tl.m_base = static_cast<int64_t>(mt) * 256;
         tl.n0 = static_cast<int64_t>(nt) * kBN;
@@ -1077,6 +1082,7 @@ nvfp4_status nvfp4_gemm_ex(const void* a_q, const void* a_sf, const float* a_s, 
     p.E = 0;
     p.sa_stride = a_s_per_row ? 1 : 0;
     p.sb_stride = b_s_per_row ? 1 : 0;
+    p.n_fast = N < M ? 1 : 0;
     const int64_t pair_tiles = ceil_div(M, 256) * p.num_n_tiles;
     if (pair_tiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
     return launch_gemm_pair<false>(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
@@ -1128,6 +1134,7 @@ nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* 
     p.E = E;
     p.sa_stride = 1;
     p.sb_stride = 1;
+    p.n_fast = 0;
     // slots: every 128-row tile of the capacity x every n-tile (about half start a pair tile)
     const int64_t slots = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     if (slots > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
