@@ -235,3 +235,13 @@ def init_data_class(kind, seed, M, K):
                     x[r, 16 * b:16 * b + 16] = v
         return to_bf16_bits(x)
     raise ValueError(kind)
+
+
+def random_bf16_bits(seed, shape, exp_lo=119, exp_hi=131):
+    """Seeded bf16 bit patterns: random sign and 7-bit mantissa, biased exponent
+    uniform in [exp_lo, exp_hi] (magnitudes 2^(exp_lo - 127) .. 2^(exp_hi - 126)).
+    A fast stand-in, at full size, for the bf16 outputs of an expert GEMM."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    r = rng.integers(0, 1 << 16, size=shape, dtype=np.uint16)
+    e = rng.integers(exp_lo, exp_hi + 1, size=shape, dtype=np.uint16)
+    return (r & np.uint16(0x807F)) | (e << np.uint16(7))

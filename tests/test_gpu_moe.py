@@ -124,7 +124,11 @@ def test_swiglu_row_count(nv):
     assert got["s"][:200].gt(0).all()
 
 
-def _grouped_case(nv, orc, T, H, N, E, k, seed, sample=None, experts_checked=None, align=128):
+def _grouped_case(nv, orc, T, H, N, E, k, seed, sample=None, align=128):
+    """Grouped GEMM over a seeded routing; every expert is checked, in full or
+    (sample) on that many random outputs plus its first and last valid rows and
+    columns.  Only the used rows of the output are read back: rows past
+    offsets[E] are not written."""
     x = W.small_matrix(seed, T, H)
     w = W.small_matrix(seed + 1, E * N, H, std=0.02).reshape(E, N, H)
     ids = _ids(seed + 2, T, E, k)
@@ -136,26 +140,29 @@ def _grouped_case(nv, orc, T, H, N, E, k, seed, sample=None, experts_checked=Non
     assert nv.nvfp4_get_device_status() == 0
     rperm = orc.moe_permute(ids, E, align, capacity=perm["capacity"])
     assert np.array_equal(perm["offsets"].cpu().numpy(), rperm["offsets"])
-    off = rperm["offsets"]
-    ra = orc.quantize(x, gather=rperm["gather"])
-    yg = bf16_to_f64(y)
-    experts = range(E) if experts_checked is None else experts_checked
-    for e in experts:
+    off, g = rperm["offsets"], rperm["gather"]
+    used = int(off[E])
+    yg = bf16_to_f64(y[:used])
+    rx = orc.quantize(x)
+    for e in range(E):
         r0, r1 = int(off[e]), int(off[e + 1])
         if r1 == r0:
             continue
-        rw = orc.quantize(w[e])
-        ae = orc.rows_of(ra, r0, r1)
+        pad = g[r0:r1] < 0
         if sample is None:
-            yref, absy = orc.gemm_exact(ae, rw, with_abs=True)
+            ae = orc.rows_of(orc.quantize(x, gather=g[r0:r1]), 0, r1 - r0)
+            yref, absy = orc.gemm_exact(ae, orc.quantize(w[e]), with_abs=True)
             check_gemm(yg[r0:r1], yref, absy, H, f"expert {e}")
         else:
             rng = np.random.default_rng(e)
-            mi = rng.integers(0, r1 - r0, sample)
-            ni = rng.integers(0, N, sample)
-            yref, absy = orc.gemm_exact_sampled(ae, rw, mi, ni)
+            rows = np.nonzero(~pad)[0]
+            mi = np.concatenate([rng.choice(rows, sample), rows[[0, -1, -1, 0]]])
+            ni = np.concatenate([rng.integers(0, N, sample), [0, N - 1, 0, N - 1]])
+            toks = g[r0 + mi]
+            ar = dict(q=rx["q"][toks], sf=rx["sf"][toks], s=rx["s"][toks])
+            idx = np.arange(mi.size)
+            yref, absy = orc.gemm_exact_sampled(ar, orc.quantize(w[e][ni]), idx, idx)
             check_gemm(yg[r0 + mi, ni], yref, absy, H, f"expert {e}")
-        pad = rperm["gather"][r0:r1] < 0
         assert not yg[r0:r1][pad].any()
 
 
@@ -172,17 +179,19 @@ def test_grouped_gemm_256_aligned(nv, orc, T, H, N, E, k):
 
 
 def test_grouped_fc1_config3_sampled_256_aligned(nv, orc):
-    _grouped_case(nv, orc, 4096, 2048, 1536, 128, 8, seed=33, sample=300,
-                  experts_checked=[0, 2, 64, 127], align=256)
+    """fc1 at the full 4096-token, 128-expert size, 256-row layout: every expert."""
+    _grouped_case(nv, orc, 4096, 2048, 1536, 128, 8, seed=33, sample=24, align=256)
 
 
 def test_grouped_fc1_config3_sampled(nv, orc):
-    """fc1 (gate+up, K=2048 -> N=1536) at the full 4096-token, 128-expert size."""
-    _grouped_case(nv, orc, 4096, 2048, 1536, 128, 8, seed=31, sample=400,
-                  experts_checked=[0, 1, 37, 64, 100, 127])
+    """fc1 (gate+up, K=2048 -> N=1536) at the full size, 128-row layout: every expert."""
+    _grouped_case(nv, orc, 4096, 2048, 1536, 128, 8, seed=31, sample=24)
 
 
 def test_grouped_fc2_config3_sampled(nv, orc):
-    """fc2 (down, K=768 -> N=2048) at the full size, on seeded expert inputs."""
-    _grouped_case(nv, orc, 4096, 768, 2048, 128, 8, seed=41, sample=400,
-                  experts_checked=[0, 5, 63, 127])
+    """fc2 (down, K=768 -> N=2048) at the full size, on seeded expert inputs: every expert."""
+    _grouped_case(nv, orc, 4096, 768, 2048, 128, 8, seed=41, sample=24)
+
+
+def test_grouped_fc2_config3_sampled_256_aligned(nv, orc):
+    _grouped_case(nv, orc, 4096, 768, 2048, 128, 8, seed=43, sample=24, align=256)
