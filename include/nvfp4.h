@@ -25,6 +25,12 @@
  *    device (a bounded wait that ran out, an out-of-range device-side index) are
  *    recorded in a per-device status word and reported by
  *    nvfp4_get_device_status().
+ *  - Calls work in the CUDA context current on the calling thread.  The device
+ *    addresses the library caches (its status word, the no-alloc permute's
+ *    scratch array) and its per-kernel attributes belong to one context: they
+ *    are looked up or set again whenever the current context differs from the
+ *    one they were taken in (another context made current, or a new primary
+ *    context after cudaDeviceReset).
  *  - The device must be compute capability 10.3 (GB300, sm_103a).
  *  - Matrix layouts are row-major with the contraction axis K contiguous
  *    (nn.Linear layout: X [M, K], W [N, K]).  bf16 data are 2-byte bfloat16.
@@ -217,18 +223,21 @@ NVFP4_API nvfp4_status nvfp4_moe_permute(
  *
  * The pages have no counterpart to this entry point; it exists for callers that
  * cannot call cudaMalloc (or any allocating routine) where they route tokens:
- * code running while a CUDA graph is captured, runtimes whose device memory is
- * owned by another allocator, or decode loops that forbid allocation on the hot
- * path.  It computes exactly what nvfp4_moe_permute computes, with the same
- * arguments minus the workspace: the per-chunk histogram scratch lives in a
- * fixed 1 MiB __device__ array inside this library, which every device that
- * loads the library holds until the process exits.
+ * runtimes whose device memory is owned by another allocator (a framework's
+ * caching allocator, a serving engine's pre-reserved pool) that nothing else
+ * may grow, and decode loops that forbid allocation on the hot path, where a
+ * cudaMalloc would synchronise the device.  It computes exactly what
+ * nvfp4_moe_permute computes, with the same arguments minus the workspace: the
+ * per-chunk histogram scratch lives in a fixed 1 MiB __device__ array inside
+ * this library, which every device that loads the library holds until the
+ * process exits.
  *
  *  Limit: nvfp4_moe_permute_workspace_bytes(tokens, topk, num_experts) must be
  *  <= 1 MiB (for 128 experts: up to 2,097,152 routed (token, slot) pairs);
  *  larger sizes return NVFP4_ERR_WORKSPACE and launch nothing.
- *  The first call on a device looks up the array's device address (with that
- *  device current) and so should come before any stream capture.
+ *  The first call on a device (and the first in each further CUDA context on
+ *  it) looks up the array's device address, with that device current, and so
+ *  should come before any stream capture.
  *  Nothing in the array needs to start at zero (every histogram entry read is
  *  first written by the same call), but every call shares it: calls that
  *  overlap on the GPU (other streams, other host threads) race and must be

@@ -988,12 +988,12 @@ bool make_map_y(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_
 template <bool kGrouped>
 nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
                               const GemmParams& p, int64_t pair_tiles, const DeviceCtx& ctx, cudaStream_t s) {
-    static bool attr_set[64] = {};
-    if (!attr_set[ctx.device & 63]) {
+    static unsigned long long attr_set[64] = {};   // per context: see ctx_cached
+    if (!ctx_cached(attr_set, ctx)) {
         if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kPSmemBytes)) != cudaSuccess)
             return NVFP4_ERR_CUDA;
-        attr_set[ctx.device & 63] = true;
+        ctx_cache_set(attr_set, ctx);
     }
     // persistent: as many pairs as can be resident at once (an SM left alone in
     // its GPC cannot host half of a pair)

@@ -201,14 +201,14 @@ nvfp4_status nvfp4_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t 
 // Permute for callers that cannot allocate device memory
 // ---------------------------------------------------------------------------
 // Some callers of this library cannot call cudaMalloc at the point where they
-// route tokens: code running while a CUDA graph is being captured, host
-// runtimes whose device memory is owned by a different allocator (a framework's
-// caching allocator, a serving engine's pre-reserved pool), or real-time
-// decode loops that forbid allocation on the hot path.  For them the routing
-// permute's scratch (per-chunk expert histograms) lives in the fixed
-// file-scope array below, which every device that loads this library keeps
-// until the process exits.  nvfp4_moe_permute itself is unchanged; this entry
-// point only supplies that array as its workspace.
+// route tokens: host runtimes whose device memory is owned by a different
+// allocator (a framework's caching allocator, a serving engine's pre-reserved
+// pool), or decode loops that forbid allocation on the hot path (cudaMalloc
+// synchronises the device).  For them the routing permute's scratch (per-chunk
+// expert histograms) lives in the fixed file-scope array below, which every
+// device that loads this library keeps until the process exits.
+// nvfp4_moe_permute itself is unchanged; this entry point only supplies that
+// array as its workspace.
 namespace nvfp4 {
 namespace {
 
@@ -217,20 +217,22 @@ static __device__ __align__(256) int32_t g_noalloc_permute_scratch[kNoAllocScrat
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64];
+unsigned long long g_noalloc_ctx[64];
 
-// Device address of the scratch array on the current device.  Looked up once
-// per device (with that device current) on the first call; the host-side name
-// of a __device__ array is not a device address, so it is never passed to a
-// kernel directly.
-nvfp4_status noalloc_scratch(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NVFP4_ERR_CUDA;
+// Device address of the scratch array in the current device's current CUDA
+// context.  Looked up (with that device current) on the first call in each
+// context -- a cudaDeviceReset or another context made current gives the array
+// another address -- and cached; the host-side name of a __device__ array is
+// not a device address, so it is never passed to a kernel directly.
+nvfp4_status noalloc_scratch(const DeviceCtx& ctx, void** out) {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    const int dev = ctx.device & 63;
+    if (!ctx_cached(g_noalloc_ctx, ctx) || g_noalloc_ptr[dev] == nullptr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_permute_scratch) != cudaSuccess || p == nullptr)
             return NVFP4_ERR_CUDA;
         g_noalloc_ptr[dev] = p;
+        ctx_cache_set(g_noalloc_ctx, ctx);
     }
     *out = g_noalloc_ptr[dev];
     return NVFP4_OK;
@@ -244,11 +246,15 @@ extern "C" nvfp4_status nvfp4_moe_permute_noalloc(const int32_t* topk_ids, int64
                                                   int32_t row_align, int32_t* expert_offsets,
                                                   int32_t* gather_rows, int64_t capacity,
                                                   int32_t* dst_rows, nvfp4_stream_t stream) {
+    // the same device checks, in the same order, as the allocating permute
+    nvfp4::DeviceCtx ctx;
+    nvfp4_status st = nvfp4::device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
     const size_t need = nvfp4_moe_permute_workspace_bytes(tokens, topk, num_experts);
     if (need == 0) return NVFP4_ERR_SHAPE;
     if (need > static_cast<size_t>(nvfp4::kNoAllocScratchBytes)) return NVFP4_ERR_WORKSPACE;
     void* scratch = nullptr;
-    const nvfp4_status st = nvfp4::noalloc_scratch(&scratch);
+    st = nvfp4::noalloc_scratch(ctx, &scratch);
     if (st != NVFP4_OK) return st;
     return nvfp4_moe_permute(topk_ids, tokens, topk, num_experts, row_align, expert_offsets,
                              gather_rows, capacity, dst_rows, scratch,

@@ -432,12 +432,12 @@ bool staged_config(int cols, int* warps, StageCfg* cfg) {
 template <int NB, int MODE>
 nvfp4_status launch_staged(const RowJob& job, int warps, StageCfg cfg, const DeviceCtx& ctx, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(warps) * cfg.depth * (cfg.row_pad + 8);
-    static bool attr[64] = {};
-    if (!attr[ctx.device & 63]) {
+    static unsigned long long attr[64] = {};   // per context: see ctx_cached
+    if (!ctx_cached(attr, ctx)) {
         if (cudaFuncSetAttribute(quant_rows_staged_kernel<NB, MODE>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024) != cudaSuccess)
             return NVFP4_ERR_CUDA;
-        attr[ctx.device & 63] = true;
+        ctx_cache_set(attr, ctx);
     }
     const int64_t want = ceil_div(job.total, warps);
     const int grid = static_cast<int>(want < ctx.sm_count ? want : ctx.sm_count);

@@ -1,8 +1,10 @@
 // status.cu -- per-device status word, size helpers and diagnostics of libnvfp4.
 //
 // The library allocates nothing: the status word is a module-scope __device__
-// variable (one per device that loads the library), reached by kernels through
-// the address cached here per device.
+// variable (one per device and CUDA context that loads the library), reached by
+// kernels through the address cached here per device and context.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -17,13 +19,46 @@ std::mutex g_mu;
 DeviceCtx g_ctx[kMaxDevices];
 nvfp4_status g_ctx_state[kMaxDevices];
 bool g_ctx_init[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id (for the process's lifetime, unlike the handle, which a new
+// context may reuse) of the context current on this thread; 0 if none is
+// current yet or the driver does not provide it.  The driver entry points come
+// through the runtime, so loading the library needs no libcuda.
+unsigned long long current_ctx_id() {
+    static const CtxGetCurrentFn get_current = []() -> CtxGetCurrentFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    static const CtxGetIdFn get_id = []() -> CtxGetIdFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<CtxGetIdFn>(p);
+    }();
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 }  // namespace
 
 nvfp4_status device_ctx(DeviceCtx* ctx) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_ctx_init[dev]) {
+    const unsigned long long id = current_ctx_id();
+    if (!g_ctx_init[dev] || id == 0 || id != g_ctx[dev].ctx_id) {
         int major = 0, minor = 0, sms = 0;
         nvfp4_status st = NVFP4_OK;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -37,7 +72,8 @@ nvfp4_status device_ctx(DeviceCtx* ctx) {
         if (st == NVFP4_OK && cudaGetSymbolAddress(&addr, g_status_words) != cudaSuccess) {
             st = NVFP4_ERR_CUDA;
         }
-        g_ctx[dev] = DeviceCtx{static_cast<unsigned*>(addr), sms, dev};
+        // the lookup above made the runtime's context current if none was
+        g_ctx[dev] = DeviceCtx{static_cast<unsigned*>(addr), sms, dev, current_ctx_id()};
         g_ctx_state[dev] = st;
         g_ctx_init[dev] = true;
     }

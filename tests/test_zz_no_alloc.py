@@ -1,6 +1,6 @@
 """The non-allocating routing permute (nvfp4_moe_permute_noalloc), for callers
-that cannot call cudaMalloc where they route tokens (graph capture, foreign
-allocators, allocation-free decode loops).  It must produce exactly what the
+that cannot call cudaMalloc where they route tokens (device memory owned by
+another allocator, allocation-free decode loops).  It must produce exactly what the
 allocating nvfp4_moe_permute produces, on consecutive calls that reuse the
 library's fixed scratch array, and refuse sizes past that array.  This file is
 collected last so a failure here leaves every other test already run.
