@@ -9,6 +9,8 @@
 // source (layout padding) becomes a zero row (zero codes, zero scales, S = 0:
 // the quantization of a zero row); the scale rows past rows_out up to a
 // multiple of 128 are zeroed, as the quantizer does.
+#include <type_traits>
+
 #include "common.cuh"
 #include "rowquant.cuh"
 
@@ -16,12 +18,15 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kGqThreads = 256;
+constexpr int kGqWarps = kGqThreads / 32;
+constexpr int kRowsPerBatch = 4;
 
 // One CTA per 128-row tile of the output (a tile of the swizzled scale layout):
 // the tile's source rows are read once into shared memory; the codes are
-// copied in 16- (or 8-) byte pieces, consecutive threads on consecutive pieces
-// of a row; each 512-byte scale atom (128 rows x one word) is written as 32
-// 16-byte lines, lane l gathering the words of rows l, l+32, l+64, l+96.
+// copied in 16- (or 8-) byte pieces, the lanes of a warp on consecutive pieces
+// of a row, four rows' loads in flight before their stores; each 512-byte
+// scale atom (128 rows x one word) is written as 32 16-byte lines, lane l
+// gathering the words of rows l, l+32, l+64, l+96.
 template <bool kVec16>
 __global__ void __launch_bounds__(kGqThreads) gather_quantized_kernel(
     const uint8_t* __restrict__ q_src, const uint8_t* __restrict__ sf_src, const float* __restrict__ s_src,
@@ -33,6 +38,14 @@ __global__ void __launch_bounds__(kGqThreads) gather_quantized_kernel(
     const int warp = threadIdx.x >> 5;
     constexpr int kPiece = kVec16 ? 16 : 8;
     const int pieces = row_bytes / kPiece;
+    using Piece = typename std::conditional<kVec16, uint4, uint2>::type;
+    auto zero_piece = []() -> Piece {
+        Piece z;
+        memset(&z, 0, sizeof(z));
+        return z;
+    };
+    auto load_piece = [](const uint8_t* row, int pc) -> Piece { return __ldg(reinterpret_cast<const Piece*>(row) + pc); };
+    auto store_piece = [](uint8_t* row, int pc, const Piece& v) { reinterpret_cast<Piece*>(row)[pc] = v; };
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t r0 = tile * 128;
         __syncthreads();                    // the previous tile's src_of is no longer read
@@ -50,21 +63,33 @@ __global__ void __launch_bounds__(kGqThreads) gather_quantized_kernel(
             src_of[threadIdx.x] = src;
         }
         __syncthreads();
-        // codes of the tile's rows (rows past rows_out have none)
-        const int64_t rows_here = rows_out - r0 < 128 ? rows_out - r0 : 128;
-        const int64_t items = rows_here * pieces;
-        for (int64_t it = threadIdx.x; it < items; it += kGqThreads) {
-            const int rr = static_cast<int>(it / pieces);
-            const int pc = static_cast<int>(it - static_cast<int64_t>(rr) * pieces);
-            const int64_t src = src_of[rr];
-            if (kVec16) {
-                const uint4 v = src >= 0 ? __ldg(reinterpret_cast<const uint4*>(q_src + src * row_bytes) + pc)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-                reinterpret_cast<uint4*>(q + (r0 + rr) * row_bytes)[pc] = v;
-            } else {
-                const uint2 v = src >= 0 ? __ldg(reinterpret_cast<const uint2*>(q_src + src * row_bytes) + pc)
-                                         : make_uint2(0u, 0u);
-                reinterpret_cast<uint2*>(q + (r0 + rr) * row_bytes)[pc] = v;
+        // codes of the tile's rows (rows past rows_out have none): warp w copies
+        // rows w, w + 8, ..., kRowsPerBatch rows at a time with every load of
+        // the batch issued before its stores (lane l on pieces l, l + 32)
+        const int rows_here = static_cast<int>(rows_out - r0 < 128 ? rows_out - r0 : 128);
+        for (int rb = warp; rb < rows_here; rb += kGqWarps * kRowsPerBatch) {
+            for (int pb = 0; pb < pieces; pb += 64) {
+                Piece v[kRowsPerBatch][2];
+#pragma unroll
+                for (int j = 0; j < kRowsPerBatch; ++j) {
+                    const int rr = rb + j * kGqWarps;
+                    const int64_t src = rr < rows_here ? src_of[rr] : -1;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int pc = pb + lane + 32 * h;
+                        v[j][h] = (src >= 0 && pc < pieces) ? load_piece(q_src + src * row_bytes, pc) : zero_piece();
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kRowsPerBatch; ++j) {
+                    const int rr = rb + j * kGqWarps;
+                    if (rr >= rows_here) continue;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int pc = pb + lane + 32 * h;
+                        if (pc < pieces) store_piece(q + (r0 + rr) * row_bytes, pc, v[j][h]);
+                    }
+                }
             }
         }
         // scale atoms: warp w builds atoms g = w, w + 8, ...; lane l writes line l

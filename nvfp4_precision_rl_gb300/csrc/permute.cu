@@ -5,8 +5,9 @@
 // "Transformer Engine path optimisation": contiguous layouts and device-side
 // metadata feed the grouped GEMM without a host round trip).
 //   1. count:   one block per chunk of kChunk pairs -> per-chunk expert histogram
-//   2. scan:    one block: per-expert totals, padded exclusive scan -> offsets,
-//               and each chunk's first row inside each expert segment
+//   2. scan:    one block of 1024 threads (experts x groups of chunks):
+//               per-expert totals, padded exclusive scan -> offsets, and each
+//               chunk's first row inside each expert segment
 //   3. scatter: one block per chunk, in order: rank inside the chunk from
 //               warp match + per-warp histograms -> gather_rows / dst_rows
 #include <mutex>
@@ -38,26 +39,57 @@ __global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t*
         counts[static_cast<int64_t>(blockIdx.x) * E + e] = s_hist[e];
 }
 
-// One block of round_up(E, 32) threads (<= 1024).
-__global__ void perm_scan_kernel(int32_t* counts, int nchunks, int E, int align, int32_t* offsets) {
+// One block of kScanThreads threads: Ew = round_up(E, 32) experts across and
+// G = kScanThreads / Ew groups of chunks down; thread (g, e) sums expert e's
+// counts over its group's chunks (loads batched so that many are in flight),
+// the first Ew threads scan the padded totals, then every thread rewrites its
+// chunks' counts as their first rows in the expert segment.
+constexpr int kScanThreads = 1024;
+constexpr int kScanBatch = 8;
+
+__global__ void __launch_bounds__(kScanThreads) perm_scan_kernel(int32_t* counts, int nchunks, int E, int align,
+                                                                 int32_t* offsets) {
+    __shared__ int32_t s_part[kScanThreads];   // [G][Ew] per-group sums, then per-group bases
     __shared__ int32_t s_warp[32];
-    const int e = threadIdx.x;
-    const int lane = e & 31, warp = e >> 5;
-    int64_t total = 0;
-    if (e < E)
-        for (int c = 0; c < nchunks; ++c) total += counts[static_cast<int64_t>(c) * E + e];
-    const int32_t padded = static_cast<int32_t>((total + align - 1) / align * align);
-    // block-wide exclusive scan of the padded segment lengths
-    int32_t incl = padded;
+    const int Ew = (E + 31) & ~31;
+    const int G = kScanThreads / Ew;
+    const int e = threadIdx.x % Ew;
+    const int g = threadIdx.x / Ew;
+    const bool mine = g < G && e < E;
+    const int per = (nchunks + G - 1) / G;
+    const int c0 = g * per;
+    const int c1 = min(c0 + per, nchunks);
+    int32_t sum = 0;
+    if (mine) {
+        for (int c = c0; c < c1; c += kScanBatch) {
+            int32_t v[kScanBatch];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
+            for (int j = 0; j < kScanBatch; ++j)
+                v[j] = (c + j < c1) ? counts[static_cast<int64_t>(c + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) sum += v[j];
+        }
     }
-    if (lane == 31) s_warp[warp] = incl;
+    if (g < G) s_part[g * Ew + e] = sum;
+    __syncthreads();
+    // the first Ew threads (whole warps): expert totals, padded, block-wide exclusive scan
+    int32_t padded = 0, incl = 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x < Ew) {
+        int64_t total = 0;
+        for (int gg = 0; gg < G; ++gg) total += s_part[gg * Ew + e];
+        padded = (e < E) ? static_cast<int32_t>((total + align - 1) / align * align) : 0;
+        incl = padded;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+    }
     __syncthreads();
     if (warp == 0) {
-        const int nw = blockDim.x >> 5;
+        const int nw = Ew >> 5;
         int32_t w = lane < nw ? s_warp[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -67,16 +99,31 @@ __global__ void perm_scan_kernel(int32_t* counts, int nchunks, int E, int align,
         if (lane < nw) s_warp[lane] = w;   // inclusive over warps
     }
     __syncthreads();
-    const int32_t excl = incl - padded + (warp > 0 ? s_warp[warp - 1] : 0);
-    if (e < E) {
+    if (threadIdx.x < Ew && e < E) {
+        const int32_t excl = incl - padded + (warp > 0 ? s_warp[warp - 1] : 0);
         offsets[e] = excl;
         if (e == E - 1) offsets[E] = excl + padded;
+        // group gg of expert e starts after the segment start and the earlier groups
         int32_t base = excl;
-        for (int c = 0; c < nchunks; ++c) {
-            const int64_t idx = static_cast<int64_t>(c) * E + e;
-            const int32_t cnt = counts[idx];
-            counts[idx] = base;
-            base += cnt;
+        for (int gg = 0; gg < G; ++gg) {
+            const int32_t part = s_part[gg * Ew + e];
+            s_part[gg * Ew + e] = base;
+            base += part;
+        }
+    }
+    __syncthreads();
+    if (mine) {
+        int32_t base = s_part[g * Ew + e];
+        for (int c = c0; c < c1; c += kScanBatch) {
+            int32_t v[kScanBatch];
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j)
+                v[j] = (c + j < c1) ? counts[static_cast<int64_t>(c + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) {
+                if (c + j < c1) counts[static_cast<int64_t>(c + j) * E + e] = base;
+                base += v[j];
+            }
         }
     }
 }
@@ -179,8 +226,7 @@ nvfp4_status nvfp4_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t 
                                                                                ctx.status);
         NVFP4_CHECK_LAUNCH();
     }
-    perm_scan_kernel<<<1, static_cast<unsigned>(round_up(E, 32)), 0, s>>>(counts, nchunks, E,
-                                                                          row_align, expert_offsets);
+    perm_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, nchunks, E, row_align, expert_offsets);
     NVFP4_CHECK_LAUNCH();
     if (nchunks > 0) {
         const size_t smem = static_cast<size_t>(E) * (1 + kPermThreads / 32) * sizeof(int32_t);
