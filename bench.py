@@ -9,8 +9,9 @@ batch (65,536 tokens, hidden 2048), the largest workload that fits one GPU:
   MoE half (Qwen3-30B-A3B experts at the same token count: 128 experts, top-8,
       524,288 routed rows): routing permute, per-token quantize of the tokens,
       copy of their quantized rows into the per-expert layout, grouped fc1
-      (2048 -> 1536), fused SwiGLU + quantize, grouped fc2 (768 -> 2048),
-      unpermute + weighted combine -> bf16 [65536, 2048].
+      (2048 -> 2 x 768) with SwiGLU in its epilogue (h bf16), per-token quantize
+      of h, grouped fc2 (768 -> 2048), unpermute + weighted combine -> bf16
+      [65536, 2048].
 The expert and QKV weights are quantized once (fixed within a step) for the
 MoE half; the dense half quantizes its weight every step.
 
@@ -266,8 +267,8 @@ class DenseLayer:
 
 class MoELayer:
     """The routed-expert step: permute, per-token quantize of the tokens, copy of
-    their quantized rows into the per-expert layout, grouped fc1, SwiGLU +
-    quantize, grouped fc2, unpermute + weighted combine."""
+    their quantized rows into the per-expert layout, grouped fc1 with the SwiGLU
+    epilogue, per-token quantize of h, grouped fc2, unpermute + weighted combine."""
 
     def __init__(self, ops, torch, dev, stream, moe, combine_weights, align):
         self.ops, self.stream = ops, stream
@@ -295,7 +296,7 @@ class MoELayer:
         self.a = dict(q=torch.empty((cap, H // 2), dtype=u8, device=dev),
                       sf=torch.empty(ops.nvfp4_sf_bytes(cap, H), dtype=u8, device=dev),
                       s=torch.empty(cap, dtype=torch.float32, device=dev))
-        self.y1 = torch.empty((cap, 2 * F), dtype=torch.bfloat16, device=dev)
+        self.h = torch.empty((cap, F), dtype=torch.bfloat16, device=dev)
         self.hq = dict(q=torch.empty((cap, F // 2), dtype=u8, device=dev),
                        sf=torch.empty(ops.nvfp4_sf_bytes(cap, F), dtype=u8, device=dev),
                        s=torch.empty(cap, dtype=torch.float32, device=dev))
@@ -325,8 +326,8 @@ class MoELayer:
             # each token's quantized row is read once from HBM (its other k - 1
             # reads hit L2) and written to its k routed rows
             "gather_quantized": T * qrow_h + R * qrow_h,
-            "grouped_fc1": R * qrow_h + w1 + R * 2 * F * 2,
-            "swiglu_quantize": R * 2 * F * 2 + R * qrow_f,
+            "grouped_fc1_swiglu": R * qrow_h + w1 + R * F * 2,
+            "quantize_h": R * F * 2 + R * qrow_f,
             "grouped_fc2": R * qrow_f + w2 + R * H * 2,
             "combine": R * H * 2 + T * k * 8 + T * H * 2,
         }
@@ -351,13 +352,15 @@ class MoELayer:
             Stage("gather_quantized", lambda: o.nvfp4_moe_gather_quantized(
                 self.xq["q"], self.xq["sf"], self.xq["s"], T, H, self.gather, cap, self.a["q"], self.a["sf"],
                 self.a["s"], s), 1, nbytes=nb["gather_quantized"], kernel="gather_quantized_kernel"),
-            Stage("grouped_fc1", lambda: o.nvfp4_grouped_gemm(
+            # fc1 (gate + up) with SwiGLU in the GEMM epilogue: h [cap, F] bf16,
+            # rows past the layout zero; then per-token quantization of h
+            Stage("grouped_fc1_swiglu", lambda: o.nvfp4_grouped_gemm_swiglu(
                 self.a["q"], self.a["sf"], self.a["s"], cap, self.off, E, self.w1["q"], self.w1["sf"],
-                self.w1["s"], 2 * F, H, self.y1, s), 1, flop=fl1, nbytes=nb["grouped_fc1"],
+                self.w1["s"], F, H, self.h, s), 1, flop=fl1, nbytes=nb["grouped_fc1_swiglu"],
                 kernel="nvfp4_gemm_pair_kernel<1>"),
-            Stage("swiglu_quantize", lambda: o.nvfp4_swiglu_quantize(
-                self.y1, cap, F, 2 * F, self.off[E:], self.hq["q"], self.hq["sf"], self.hq["s"], None, s), 1,
-                nbytes=nb["swiglu_quantize"], kernel="swiglu_quant_kernel"),
+            Stage("quantize_h", lambda: o.nvfp4_quantize_per_token(
+                self.h, cap, F, F, None, cap, o.PER_TOKEN, self.hq["q"], self.hq["sf"], self.hq["s"], stream=s), 1,
+                nbytes=nb["quantize_h"], kernel="quant_rows_staged_kernel"),
             Stage("grouped_fc2", lambda: o.nvfp4_grouped_gemm(
                 self.hq["q"], self.hq["sf"], self.hq["s"], cap, self.off, E, self.w2["q"], self.w2["sf"],
                 self.w2["s"], H, F, self.y2, s), 1, flop=fl2, nbytes=nb["grouped_fc2"],

@@ -350,6 +350,33 @@ NVFP4_API nvfp4_status nvfp4_grouped_gemm(
     const void* b_q, const void* b_sf, const float* b_s, int64_t N, int64_t K,
     void* y, nvfp4_stream_t stream);
 
+/*
+ * Grouped W4A4 GEMM of a SwiGLU expert's fused gate + up projection with the
+ * SwiGLU in its epilogue: for every expert e and row m of its segment,
+ *     g[m, j] = Y[m, j],  u[m, j] = Y[m, F + j]    (Y as nvfp4_grouped_gemm
+ *                                                   computes it, rounded to bf16)
+ *     h[m, j] = bf16(silu(g) * u)                  (j < F)
+ * -- the same bits as nvfp4_grouped_gemm with N = 2F followed by
+ * nvfp4_swiglu_quantize's h, without writing or re-reading Y ("Towards
+ * Blackwell-Native 8-bit and 4-bit RL", "Parallelism and tensor-conversion
+ * consistency contract": gate and up are one fused GEMM in a SwiGLU MoE layer;
+ * the gate is the first half).  A pair tile multiplies gate rows n0 .. n0+127
+ * and the matching up rows F+n0 .. of B, so no weight reordering is needed.
+ *
+ *  a_*, rows_capacity, expert_offsets, E   as for nvfp4_grouped_gemm.
+ *  b_q, b_sf, b_s   expert weights with 2F rows each (gate rows 0..F-1, up rows
+ *                   F..2F-1), laid out as for nvfp4_grouped_gemm with N = 2F.
+ *  ffn              F; F % 128 == 0, K % 64 == 0.
+ *  h                bf16 [rows_capacity, F]; rows >= expert_offsets[E] are
+ *                   written as zeros (so a per-token quantization of all
+ *                   rows_capacity rows gives zero rows there).
+ */
+NVFP4_API nvfp4_status nvfp4_grouped_gemm_swiglu(
+    const void* a_q, const void* a_sf, const float* a_s, int64_t rows_capacity,
+    const int32_t* expert_offsets, int32_t E,
+    const void* b_q, const void* b_sf, const float* b_s, int64_t ffn, int64_t K,
+    void* h, nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Unpermute + weighted combine (after the MoE fc2)                          */
 /* ------------------------------------------------------------------------- */

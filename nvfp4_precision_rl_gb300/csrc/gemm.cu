@@ -50,6 +50,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "swiglu.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -116,6 +117,14 @@ struct GemmParams {
     int sa_stride;            // 1: S_a per row of A; 0: one S_a for all rows
     int sb_stride;            // 1: S_b per row of B; 0: one S_b for all rows
     int n_fast;               // dense: 1 walks the tiles n-tile fastest, 0 m-tile fastest
+    // Grouped SwiGLU epilogue (fc1 of a SwiGLU expert): B holds each expert's
+    // F gate rows then its F up rows; a pair tile pairs gate rows n0 .. n0+127
+    // (even CTA) with up rows F+n0 .. (odd CTA), and its epilogue writes
+    // h = bf16(silu(g) u) for output columns n0 .. n0+127 of H [rows, F].
+    int swiglu;               // 0 or 1
+    int64_t ffn;              // swiglu: F (= N, the output columns)
+    int64_t b_rows;           // rows of B per expert: N, or 2F with swiglu
+    int n_step;               // output columns per tile: 256, or 128 with swiglu
 };
 
 // ----------------------------------------------------------------------------
@@ -281,6 +290,13 @@ constexpr int kRegsLaunch = 128;
 constexpr int kRegsWG0 = 64;
 constexpr int kRegsWG1 = 80;
 constexpr int kRegsEpi = 184;
+// The SwiGLU epilogue holds fewer accumulator registers (it pairs 64 gate with
+// 64 up columns) and its tile scheduler more index arithmetic: 80 / 80 / 168.
+constexpr int kRegsWG0Swi = 80;
+constexpr int kRegsWG1Swi = 80;
+constexpr int kRegsEpiSwi = 168;
+static_assert(128 * kRegsWG0Swi + 128 * kRegsWG1Swi + 256 * kRegsEpiSwi <= kPThreads * kRegsLaunch,
+              "register split exceeds the launch's registers");
 static_assert(kPThreads == 512, "four warpgroups");
 static_assert(128 * kRegsWG0 + 128 * kRegsWG1 + 256 * kRegsEpi <= kPThreads * kRegsLaunch,
               "register split exceeds the launch's registers");
@@ -405,7 +421,7 @@ struct PairTile {
 // 128-row tile of an expert's segment, so an expert with an odd number of
 // tiles ends in a tile whose odd CTA reads rows past the expert (its results
 // are computed with this expert's B and never stored).
-template <bool kGrouped>
+template <bool kGrouped, bool kSwiGLU>
 __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int num_pm, int mrows) {
     PairTile tl;
     if (!kGrouped) {
@@ -421,6 +437,7 @@ __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int
     }
     const int nt = t % p.num_n_tiles;
     const int64_t m0 = static_cast<int64_t>(t / p.num_n_tiles) * mrows;
+    const int64_t n0 = static_cast<int64_t>(nt) * (kSwiGLU ? 128 : kBN);
     // The last expert e with offsets[e] <= m0 (empty experts are passed over),
     // i.e. (the number of e < E with offsets[e] <= m0) - 1 for nondecreasing
     // offsets, found in two rounds of independent loads -- the first entry of
@@ -453,14 +470,14 @@ __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int
         }
     tl.run = mrows == 256 || (((m0 - e_begin) >> 7) & 1) == 0;
     tl.m_base = m0;
-    tl.n0 = static_cast<int64_t>(nt) * kBN;
-    tl.b_row0 = static_cast<int64_t>(lo) * p.N + tl.n0;
+    tl.n0 = n0;
+    tl.b_row0 = static_cast<int64_t>(lo) * p.b_rows + n0;
     tl.row_end = e_end;
     tl.expert = lo;
     return tl;
 }
 
-template <bool kGrouped>
+template <bool kGrouped, bool kSwiGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                            const __grid_constant__ CUtensorMap tma_b,
@@ -530,6 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     pdl_wait();             // the producers of the operands and offsets have completed
     int tiles = num_pm * p.num_n_tiles;
     int mrows = 128;   // grouped: rows per slot of the padded layout
+    int64_t used = p.M;   // grouped: rows of the layout in use (offsets[E])
     if (kGrouped) {
         // A layout whose expert segments are all 256-row aligned is walked in
         // 256-row slots, every one a pair tile (the strided assignment then
@@ -539,7 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         for (int e = threadIdx.x; e <= p.E; e += blockDim.x) misaligned |= (__ldg(p.offsets + e) & 255) != 0;
         mrows = __syncthreads_or(misaligned) ? 128 : 256;
         // slots of the padded layout in use: it ends at offsets[E]
-        int64_t used = __ldg(p.offsets + p.E);
+        used = __ldg(p.offsets + p.E);
         if (used > p.M || used < 0) {
             if (threadIdx.x == 0) record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
             used = used < 0 ? 0 : p.M;
@@ -551,7 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // split (every warp of the warpgroup executes it, converged), so the code
     // of the branch is compiled within that register count.
     if (warp < kFirstSFWarp) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG0));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwiGLU ? kRegsWG0Swi : kRegsWG0));
         if ((warp == 0 || warp == kPBWarp) && lane < kPLoadLanes) {
             // ------------------------------ producers (both CTAs) ------------------
             // Warp 0 loads A and its scales, warp kPBWarp this CTA's 128 rows of B
@@ -566,7 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm, mrows);
+                const PairTile tl = pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows);
                 if (!tl.run) continue;
                 if (kGrouped && !side_b && rank == 0 && (__ldg(p.offsets + tl.expert) & 127) != 0)
                     record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
@@ -574,8 +592,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 const int64_t n0 = tl.n0;
                 const int a_tile = static_cast<int>(m0 / 128);
                 const bool a_sf_ok = a_tile < a_row_tiles;
+                // the B tile's two 128-row halves and their scale-atom columns:
+                // consecutive rows, or (SwiGLU) gate rows and the matching up rows
                 const int nt128 = static_cast<int>(n0 / 128);
-                const bool two_b_atoms = nt128 + 1 < sfb_tiles_n;
+                const int64_t b_half1 = kSwiGLU ? p.ffn : 128;
+                const int atom1 = nt128 + static_cast<int>(b_half1 / 128);
+                const bool two_b_atoms = kSwiGLU || atom1 < sfb_tiles_n;
                 const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     ok = __all_sync(kPLoadMask,
@@ -598,14 +620,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                                       sf_bytes, &full[stage]);
                     } else {
                         tma_load_2d(map, &full[stage], sB + stage * kPBHalfBytes + sub * kPBoxRows * kBKBytes,
-                                    kt * kBKBytes, static_cast<int32_t>(tl.b_row0 + rank * 128 + kPBoxRows * sub));
+                                    kt * kBKBytes,
+                                    static_cast<int32_t>(tl.b_row0 + rank * b_half1 + kPBoxRows * sub));
                         if (sub == 0) {
                             bulk_load(sSFB + stage * kSFBTileBytes,
                                       sfb_e + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
                                       &full[stage]);
                             if (two_b_atoms)
                                 bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
-                                          sfb_e + (static_cast<int64_t>(nt128 + 1) * p.kgroups + g0) * kSFAtomBytes,
+                                          sfb_e + (static_cast<int64_t>(atom1) * p.kgroups + g0) * kSFAtomBytes,
                                           sf_bytes, &full[stage]);
                         }
                     }
@@ -635,7 +658,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const uint64_t a_desc0 = sw128_desc(sA);
             const uint64_t b_desc0 = sw128_desc(sB);
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (mrows != 256 && !pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
+                if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows).run) continue;
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
@@ -693,7 +716,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t slot = 0, phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                const PairTile tl = pair_tile_at<kGrouped>(p, t, num_pm, mrows);
+                const PairTile tl = pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows);
                 if (!tl.run) continue;
                 const int64_t mrow0 = tl.m_base + rank * 128;
                 float a[128 / 32], b[kBN / 32];
@@ -702,12 +725,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     const int64_t m = mrow0 + i * 32 + lane;
                     a[i] = (m < p.M) ? __ldg(p.sa + m * p.sa_stride) : 0.0f;
                 }
+                // the tile's 256 B rows: consecutive, or (SwiGLU) 128 gate rows
+                // then the 128 matching up rows
                 const float* sbp =
-                    p.sb + p.sb_stride * ((kGrouped ? static_cast<int64_t>(tl.expert) * p.N : 0) + tl.n0);
+                    p.sb + p.sb_stride * ((kGrouped ? static_cast<int64_t>(tl.expert) * p.b_rows : 0) + tl.n0);
     #pragma unroll
                 for (int i = 0; i < kBN / 32; ++i) {
-                    const int64_t n = tl.n0 + i * 32 + lane;
-                    b[i] = (n < p.N) ? __ldg(sbp + (i * 32 + lane) * p.sb_stride) : 0.0f;
+                    const int c = i * 32 + lane;
+                    if (kSwiGLU) {
+                        b[i] = __ldg(sbp + (c < 128 ? c : p.ffn + c - 128) * p.sb_stride);
+                    } else {
+                        const int64_t n = tl.n0 + c;
+                        b[i] = (n < p.N) ? __ldg(sbp + c * p.sb_stride) : 0.0f;
+                    }
                 }
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&info_empty[slot], phase ^ 1u, kWaitLimitNs, abort_flag));
                 if (!ok) break;
@@ -744,14 +774,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
         }
     } else if (warp < kFirstEpiWarp) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWG1));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwiGLU ? kRegsWG1Swi : kRegsWG1));
             // ------------------------------ scale warps (both CTAs) ----------------
             const int quad = warp & 3;
             const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (mrows != 256 && !pair_tile_at<kGrouped>(p, t, num_pm, mrows).run) continue;
+                if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows).run) continue;
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
                     got = __all_sync(0xFFFFFFFFu, got);
@@ -792,17 +822,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 if (lane == 0) record_error(p.status, NVFP4_ERR_TIMEOUT, DETAIL_GEMM_MMA);
             }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSwiGLU ? kRegsEpiSwi : kRegsEpi));
             // ------------------------------ epilogue (both CTAs) -------------------
             // Warp (quad, half) owns TMEM lanes quad*32.. and accumulator columns
             // half*128..: two rounds of 64 columns, each loaded with two tcgen05.ld
             // and one wait, scaled by S_a[m] S_b[n], rounded to bf16, written into
             // this warp's swizzled 32 x 64 staging box and stored by TMA (which
-            // clips rows >= M and columns >= N).
+            // clips rows >= M and columns >= N).  With the SwiGLU epilogue the
+            // warp instead loads gate columns half*64.. and the matching up
+            // columns 128 + half*64.., rounds both to bf16 as the plain epilogue
+            // would, and stores the 64 columns h = bf16(silu(g) u) of one box.
             const int quad = warp & 3;
             const int ew = warp - kFirstEpiWarp;
             const int half = ew >> 2;
-            const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + half * (kBN / 2);
+            const uint32_t t_lanes = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+            // accumulator columns of the four 32-column loads
+            const uint32_t c_first = kSwiGLU ? half * 64 : half * (kBN / 2);
+            const uint32_t c_second = kSwiGLU ? 128 + half * 64 : half * (kBN / 2) + 64;
             uint8_t* box = sOut + ew * kPOutBoxBytes;
             uint8_t* my_row = box + lane * 128;
             const uint32_t acc_empty_leader = peer_addr(acc_empty, 0);
@@ -828,11 +864,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     write = ti->write != 0;
                     row0 = ti->m_base + rank * 128 + quad * 32;
                     sa = ti->sa[quad * 32 + lane];
-                    n_half = ti->n0 + half * (kBN / 2);
-                    sb_s = ti->sb + half * (kBN / 2);
+                    n_half = ti->n0 + half * (kSwiGLU ? 64 : kBN / 2);
+                    sb_s = ti->sb + half * (kSwiGLU ? 64 : kBN / 2);
                 } else {
                     if (t >= tiles) break;
-                    const PairTile tl = pair_tile_at<false>(p, t, num_pm, mrows);
+                    const PairTile tl = pair_tile_at<false, false>(p, t, num_pm, mrows);
                     t += npairs;
                     // this CTA's 128 rows lie inside the tile's row range, or wholly past it
                     write = tl.m_base + rank * 128 < tl.row_end;
@@ -886,10 +922,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 // accumulator released at once; scaling, staging and the stores
                 // (two 64-column boxes) follow while the next tile's MMAs run.
                 uint32_t r0[32], r1[32], r2[32], r3[32];
-                tmem_ld32(t_base, r0);
-                tmem_ld32(t_base + 32, r1);
-                tmem_ld32(t_base + 64, r2);
-                tmem_ld32(t_base + 96, r3);
+                tmem_ld32(t_lanes + c_first, r0);
+                tmem_ld32(t_lanes + c_first + 32, r1);
+                tmem_ld32(t_lanes + c_second, r2);
+                tmem_ld32(t_lanes + c_second + 32, r3);
                 tmem_wait(r0);
                 reg_fence(r1);
                 reg_fence(r2);
@@ -898,6 +934,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+                if constexpr (kGrouped && kSwiGLU) {
+                    // g and u as the plain epilogue rounds them, then h = bf16(silu(g) u)
+                    uint32_t qa[16], qb[16];
+                    {
+                        uint32_t qg[16], qu[16];
+                        scale_chunk(r0, sb_s, sa, qg);
+                        scale_chunk(r2, sb_s + 128, sa, qu);
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) qa[j] = swiglu_pair(qg[j], qu[j]);
+                    }
+                    {
+                        uint32_t qg[16], qu[16];
+                        scale_chunk(r1, sb_s + 32, sa, qg);
+                        scale_chunk(r3, sb_s + 160, sa, qu);
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) qb[j] = swiglu_pair(qg[j], qu[j]);
+                    }
+                    // every read of this tile's ring slot is done
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&info_empty[islot]);
+                    stage(qa, qb);
+                    store(n_half);
+                } else {
                 {
                     uint32_t qa[16], qb[16];
                     scale_chunk(r0, sb_s, sa, qa);
@@ -917,11 +976,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     stage(qa, qb);
                     store(n_half + 64);
                 }
+                }
                 acc_phase ^= 1u;
                 if (kGrouped && ++islot == kInfoSlots) {
                     islot = 0;
                     iphase ^= 1u;
                 }
+            }
+            // SwiGLU: the rows of H past the layout's used rows (no tile covers
+            // them) are written as zeros, each CTA a slice, 16 bytes per lane
+            if (kGrouped && kSwiGLU && used < p.M) {
+                const int64_t tail = p.M - used;
+                const int64_t per = (tail + gridDim.x - 1) / gridDim.x;
+                const int64_t r_begin = used + static_cast<int64_t>(blockIdx.x) * per;
+                const int64_t r_end = r_begin + per < p.M ? r_begin + per : p.M;
+                const int pieces = static_cast<int>(p.ffn / 8);
+                for (int64_t r = r_begin + ew; r < r_end; r += kEpiWarps)
+                    for (int c = lane; c < pieces; c += 32)
+                        reinterpret_cast<uint4*>(p.y + r * p.ld_y)[c] = make_uint4(0u, 0u, 0u, 0u);
             }
             // the staging boxes stay valid until the stores have finished
             if (lane == 0) bulk_wait_all();
@@ -985,12 +1057,12 @@ bool make_map_y(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGrouped>
+template <bool kGrouped, bool kSwiGLU>
 nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
                               const GemmParams& p, int64_t pair_tiles, const DeviceCtx& ctx, cudaStream_t s) {
     static unsigned long long attr_set[64] = {};   // per context: see ctx_cached
     if (!ctx_cached(attr_set, ctx)) {
-        if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kPSmemBytes)) != cudaSuccess)
             return NVFP4_ERR_CUDA;
         ctx_cache_set(attr_set, ctx);
@@ -1004,7 +1076,7 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
         cfg.blockDim = dim3(kPThreads, 1, 1);
         cfg.dynamicSmemBytes = kPSmemBytes;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel<kGrouped>, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU>, &cfg) != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
             n = ctx.sm_count / 2;
         }
@@ -1025,7 +1097,7 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_pair_kernel<kGrouped>, ma, mb, my, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU>, ma, mb, my, p) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return NVFP4_OK;
 }
@@ -1083,9 +1155,13 @@ nvfp4_status nvfp4_gemm_ex(const void* a_q, const void* a_sf, const float* a_s, 
     p.sa_stride = a_s_per_row ? 1 : 0;
     p.sb_stride = b_s_per_row ? 1 : 0;
     p.n_fast = N < M ? 1 : 0;
+    p.swiglu = 0;
+    p.ffn = 0;
+    p.b_rows = N;
+    p.n_step = kBN;
     const int64_t pair_tiles = ceil_div(M, 256) * p.num_n_tiles;
     if (pair_tiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
-    return launch_gemm_pair<false>(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_pair<false, false>(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int64_t M,
@@ -1094,16 +1170,24 @@ nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int
     return nvfp4_gemm_ex(a_q, a_sf, a_s, 1, M, b_q, b_sf, b_s, 1, N, K, y, ld_y, stream);
 }
 
-nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* a_s,
-                                int64_t rows_capacity, const int32_t* expert_offsets, int32_t E,
-                                const void* b_q, const void* b_sf, const float* b_s, int64_t N,
-                                int64_t K, void* y, nvfp4_stream_t stream) {
+}  // extern "C"
+
+namespace nvfp4 {
+namespace {
+
+// The grouped GEMM, plain (Y [rows, N]) or with the SwiGLU epilogue
+// (H [rows, F], N = F, B rows per expert 2F).
+nvfp4_status grouped_gemm(const void* a_q, const void* a_sf, const float* a_s, int64_t rows_capacity,
+                          const int32_t* expert_offsets, int32_t E, const void* b_q, const void* b_sf,
+                          const float* b_s, int64_t N, int64_t K, void* y, bool swiglu, cudaStream_t stream) {
     DeviceCtx ctx;
     nvfp4_status st = device_ctx(&ctx);
     if (st != NVFP4_OK) return st;
     if (rows_capacity < 0 || rows_capacity > (int64_t(1) << 31) - kBM) return NVFP4_ERR_SHAPE;
     if (E < 1 || E > 1024) return NVFP4_ERR_SHAPE;
-    if ((st = check_operand_shapes(N, K)) != NVFP4_OK) return st;
+    const int64_t b_rows = swiglu ? 2 * N : N;
+    if ((st = check_operand_shapes(b_rows, K)) != NVFP4_OK) return st;
+    if (swiglu && N % 128 != 0) return NVFP4_ERR_SHAPE;
     if (rows_capacity == 0) return NVFP4_OK;
     if (!a_q || !a_sf || !a_s || !expert_offsets || !b_q || !b_sf || !b_s || !y)
         return NVFP4_ERR_INVALID_ARG;
@@ -1112,7 +1196,7 @@ nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* 
         return NVFP4_ERR_ALIGNMENT;
     CUtensorMap ma, mb, my;
     if (!make_map(&ma, a_q, rows_capacity, K / 2, kPBoxRows) ||
-        !make_map(&mb, b_q, static_cast<int64_t>(E) * N, K / 2, kPBoxRows) ||
+        !make_map(&mb, b_q, static_cast<int64_t>(E) * b_rows, K / 2, kPBoxRows) ||
         !make_map_y(&my, y, rows_capacity, N, N))
         return NVFP4_ERR_CUDA;
     GemmParams p;
@@ -1126,19 +1210,45 @@ nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* 
     p.M = rows_capacity;
     p.N = N;
     p.ld_y = N;
-    p.sfb_expert_bytes = static_cast<int64_t>(nvfp4_sf_bytes(N, K));
+    p.sfb_expert_bytes = static_cast<int64_t>(nvfp4_sf_bytes(b_rows, K));
     p.kgroups = static_cast<int>(K / 64);
     p.num_k_tiles = static_cast<int>(ceil_div(K, 256));
-    p.num_n_tiles = static_cast<int>(ceil_div(N, kBN));
+    p.n_step = swiglu ? 128 : kBN;
+    p.num_n_tiles = static_cast<int>(ceil_div(N, p.n_step));
     p.num_m_tiles = static_cast<int>(ceil_div(rows_capacity, kBM));
     p.E = E;
     p.sa_stride = 1;
     p.sb_stride = 1;
     p.n_fast = 0;
+    p.swiglu = swiglu ? 1 : 0;
+    p.ffn = swiglu ? N : 0;
+    p.b_rows = b_rows;
     // slots: every 128-row tile of the capacity x every n-tile (about half start a pair tile)
     const int64_t slots = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     if (slots > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
-    return launch_gemm_pair<true>(ma, mb, my, p, (slots + 1) / 2, ctx, reinterpret_cast<cudaStream_t>(stream));
+    return swiglu ? launch_gemm_pair<true, true>(ma, mb, my, p, (slots + 1) / 2, ctx, stream)
+                  : launch_gemm_pair<true, false>(ma, mb, my, p, (slots + 1) / 2, ctx, stream);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" {
+
+nvfp4_status nvfp4_grouped_gemm(const void* a_q, const void* a_sf, const float* a_s,
+                                int64_t rows_capacity, const int32_t* expert_offsets, int32_t E,
+                                const void* b_q, const void* b_sf, const float* b_s, int64_t N,
+                                int64_t K, void* y, nvfp4_stream_t stream) {
+    return grouped_gemm(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_sf, b_s, N, K, y, false,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_grouped_gemm_swiglu(const void* a_q, const void* a_sf, const float* a_s,
+                                       int64_t rows_capacity, const int32_t* expert_offsets, int32_t E,
+                                       const void* b_q, const void* b_sf, const float* b_s, int64_t ffn,
+                                       int64_t K, void* h, nvfp4_stream_t stream) {
+    return grouped_gemm(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_sf, b_s, ffn, K, h, true,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -107,8 +107,15 @@ struct RowJob {
     int64_t total;      // row slots of both
 };
 
+// Rows of up to 96 blocks (1536 columns) fit 64 registers per thread, so two
+// CTAs share an SM when their row buffers fit: a warp's rows are a chain of
+// dependent steps (wait, amax, the exact scale divides, encode), and more warps
+// per SM keep more rows in flight.
+template <int NB>
+constexpr int staged_ctas_per_sm() { return NB <= 3 ? 2 : 1; }
+
 template <int NB, int MODE>
-__global__ void __launch_bounds__(512, 1) quant_rows_staged_kernel(RowJob job, StageCfg cfg) {
+__global__ void __launch_bounds__(512, staged_ctas_per_sm<NB>()) quant_rows_staged_kernel(RowJob job, StageCfg cfg) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_launch_dependents();    // a dependent waits for this grid's completion itself
     const int lane = threadIdx.x & 31;
@@ -440,7 +447,9 @@ nvfp4_status launch_staged(const RowJob& job, int warps, StageCfg cfg, const Dev
         ctx_cache_set(attr, ctx);
     }
     const int64_t want = ceil_div(job.total, warps);
-    const int grid = static_cast<int>(want < ctx.sm_count ? want : ctx.sm_count);
+    const int per_sm = (staged_ctas_per_sm<NB>() == 2 && 2 * smem <= 220 * 1024) ? 2 : 1;
+    const int64_t cap = static_cast<int64_t>(ctx.sm_count) * per_sm;
+    const int grid = static_cast<int>(want < cap ? want : cap);
     quant_rows_staged_kernel<NB, MODE><<<grid, warps * 32, smem, s>>>(job, cfg);
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;

@@ -58,6 +58,7 @@ def lib():
         "nvfp4_moe_permute_noalloc": (st, [P, I64, I32, I32, I32, P, P, I64, P, P]),
         "nvfp4_gemm": (st, [P, P, P, I64, P, P, P, I64, I64, P, I64, P]),
         "nvfp4_grouped_gemm": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
+        "nvfp4_grouped_gemm_swiglu": (st, [P, P, P, I64, P, I32, P, P, P, I64, I64, P, P]),
         "nvfp4_swiglu_quantize": (st, [P, I64, I64, I64, P, P, P, P, P, P]),
         "nvfp4_dequantize": (st, [P, P, P, ctypes.c_int32, I64, I64, P, I64, P]),
         "nvfp4_gemm_ex": (st, [P, P, P, ctypes.c_int32, I64, P, P, P, ctypes.c_int32, I64, I64, P, I64, P]),
@@ -156,6 +157,13 @@ def nvfp4_grouped_gemm(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_
     _ok("nvfp4_grouped_gemm", lib().nvfp4_grouped_gemm(
         _p(a_q), _p(a_sf), _p(a_s), rows_capacity, _p(expert_offsets), E, _p(b_q), _p(b_sf),
         _p(b_s), N, K, _p(y), _s(stream)))
+
+
+def nvfp4_grouped_gemm_swiglu(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_sf, b_s, ffn, K, h,
+                              stream=None):
+    _ok("nvfp4_grouped_gemm_swiglu", lib().nvfp4_grouped_gemm_swiglu(
+        _p(a_q), _p(a_sf), _p(a_s), rows_capacity, _p(expert_offsets), E, _p(b_q), _p(b_sf), _p(b_s), ffn, K,
+        _p(h), _s(stream)))
 
 
 def nvfp4_moe_combine(y2, rows, ld_y2, dst_rows, weights, tokens, topk, hidden, out, ld_out, stream=None):
@@ -386,6 +394,16 @@ def grouped_gemm(a, expert_offsets, num_experts, b_q, b_sf, b_s, N, K, out=None,
     nvfp4_grouped_gemm(a["q"], a["sf"], a["s"], rows, expert_offsets, num_experts, b_q, b_sf, b_s,
                        N, K, y, stream)
     return y
+
+
+def grouped_gemm_swiglu(a, expert_offsets, num_experts, b_q, b_sf, b_s, ffn, K, out=None, stream=None):
+    """h [rows, ffn] bf16 = bf16(silu(g) u) of the grouped fc1 product whose
+    first ffn columns are the gate g and the next ffn the up projection u."""
+    rows = a["rows"]
+    h = out if out is not None else torch.empty((rows, ffn), dtype=torch.bfloat16, device=a["q"].device)
+    nvfp4_grouped_gemm_swiglu(a["q"], a["sf"], a["s"], rows, expert_offsets, num_experts, b_q, b_sf, b_s, ffn, K,
+                              h, stream)
+    return h
 
 
 def moe_combine(y2, dst_rows, weights, out=None, stream=None):

@@ -195,3 +195,74 @@ def test_grouped_fc2_config3_sampled(nv, orc):
 
 def test_grouped_fc2_config3_sampled_256_aligned(nv, orc):
     _grouped_case(nv, orc, 4096, 768, 2048, 128, 8, seed=43, sample=24, align=256)
+
+
+def _silu_h_bound(g, u, dg, du):
+    """|h - silu(g) u| allowed when g and u are each off by dg, du, plus one bf16
+    ulp of h and binary32 evaluation slack: silu'(g) = s (1 + g (1 - s)), s = sigma(g)."""
+    s = 1.0 / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    h = g * s * u
+    dsilu = np.abs(s * (1.0 + g * (1.0 - s)))
+    return np.abs(u) * dsilu * dg + np.abs(g * s) * du + 2.0 * bf16_ulp(h) + 1e-6 * np.abs(h)
+
+
+def _swiglu_case(nv, orc, T, H, F, E, k, seed, align, sample=None):
+    """fc1 with the SwiGLU epilogue: (1) the same bits as the grouped GEMM
+    followed by the SwiGLU kernel's h; rows past offsets[E] zero; (2) h within
+    the GEMM tolerance, carried through silu(g) u, of the exact product."""
+    x = W.small_matrix(seed, T, H)
+    w = W.small_matrix(seed + 1, E * 2 * F, H, std=0.02).reshape(E, 2 * F, H)
+    ids = _ids(seed + 2, T, E, k)
+    perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E, row_align=align)
+    a = nv.quantize(to_dev(x), gather=perm["gather"])
+    wq = nv.quantize_experts(to_dev(w.reshape(E * 2 * F, H)).reshape(E, 2 * F, H))
+    y1 = nv.grouped_gemm(a, perm["offsets"], E, wq["q"], wq["sf"], wq["s"], 2 * F, H)
+    ref = nv.swiglu_quantize(y1, F, row_count=perm["offsets"][E:], want_h=True)
+    h = torch.full((a["rows"], F), 7, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    nv.grouped_gemm_swiglu(a, perm["offsets"], E, wq["q"], wq["sf"], wq["s"], F, H, out=h)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_status() == 0
+    used = int(perm["offsets"][E].item())
+    assert torch.equal(h[:used].view(torch.int16), ref["h"][:used].view(torch.int16)), \
+        "SwiGLU epilogue differs from the grouped GEMM + SwiGLU kernel"
+    assert not h[used:].view(torch.int16).any(), "rows past the layout not zero"
+    # against the oracle's exact products
+    rperm = orc.moe_permute(ids, E, align, capacity=perm["capacity"])
+    off, g = rperm["offsets"], rperm["gather"]
+    rx = orc.quantize(x)
+    hb = bf16_to_f64(h[:used])
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        rows = np.nonzero(g[r0:r1] >= 0)[0]
+        rng = np.random.default_rng(100 + e)
+        n = rows.size * F if sample is None else sample
+        mi = rows[rng.integers(0, rows.size, n)] if sample else np.repeat(rows, F)
+        ji = rng.integers(0, F, n) if sample else np.tile(np.arange(F), rows.size)
+        toks = g[r0 + mi]
+        ar = dict(q=rx["q"][toks], sf=rx["sf"][toks], s=rx["s"][toks])
+        idx = np.arange(n)
+        gq = orc.quantize(w[e][ji])
+        uq = orc.quantize(w[e][F + ji])
+        gr, ga = orc.gemm_exact_sampled(ar, gq, idx, idx)
+        ur, ua = orc.gemm_exact_sampled(ar, uq, idx, idx)
+        dg = bf16_ulp(gr) + 4.0 * H * 2.0 ** -24 * ga
+        du = bf16_ulp(ur) + 4.0 * H * 2.0 ** -24 * ua
+        s = 1.0 / (1.0 + np.exp(-np.clip(gr, -700, 700)))
+        hx = gr * s * ur
+        got = hb[r0 + mi, ji]
+        bad = np.abs(got - hx) > _silu_h_bound(gr, ur, dg, du)
+        assert not bad.any(), f"expert {e}: {bad.sum()} h values outside the carried GEMM tolerance"
+
+
+@pytest.mark.parametrize("T,H,F,E,k,align", [(300, 256, 128, 16, 4, 128), (200, 512, 256, 8, 2, 256),
+                                             (64, 192, 384, 4, 1, 128)])
+def test_grouped_swiglu_small(nv, orc, T, H, F, E, k, align):
+    _swiglu_case(nv, orc, T, H, F, E, k, seed=T + F, align=align)
+
+
+def test_grouped_swiglu_config3(nv, orc):
+    """fc1 (2048 -> 2 x 768) with the SwiGLU epilogue at 4096 tokens, 128
+    experts, top-8, 256-row layout; every expert sampled."""
+    _swiglu_case(nv, orc, 4096, 2048, 768, 128, 8, seed=61, align=256, sample=24)

@@ -121,6 +121,25 @@ def test_grouped_fc1_rollout_every_expert(nv, orc, rollout):
                           2 * m.ffn, m.hidden, seed=51)
 
 
+def test_grouped_swiglu_rollout(nv, rollout):
+    """fc1 with the SwiGLU epilogue at full size: the same bits as the grouped
+    GEMM followed by the SwiGLU kernel (each checked against the oracle here and
+    in the MoE tests), rows past the layout zero."""
+    m = rollout["m"]
+    E, F, H = m.experts, m.ffn, m.hidden
+    wq = nv.quantize_experts(to_dev(m.w1.reshape(E * 2 * F, H)).reshape(E, 2 * F, H))
+    off = rollout["perm"]["offsets"]
+    y1 = nv.grouped_gemm(rollout["a"], off, E, wq["q"], wq["sf"], wq["s"], 2 * F, H)
+    ref = nv.swiglu_quantize(y1, F, row_count=off[E:], want_h=True)
+    del y1
+    h = nv.grouped_gemm_swiglu(rollout["a"], off, E, wq["q"], wq["sf"], wq["s"], F, H)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_status() == 0
+    used = int(rollout["rperm"]["offsets"][-1])
+    assert torch.equal(h[:used].view(torch.int16), ref["h"][:used].view(torch.int16))
+    assert not h[used:].view(torch.int16).any()
+
+
 def test_grouped_fc2_rollout_every_expert(nv, orc, rollout):
     """fc2 on seeded expert inputs h [65536, 768] (quantized once, copied to the
     layout by the same permutation)."""
