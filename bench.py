@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--sections", default="c4,c2,c3",
                     help="extra sections after the headline: c4, c2, c3 (comma list, or 'none')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sections-only", action="store_true",
+                    help="run only the extra sections (small cases for profiling); prints their JSON")
     ap.add_argument("--moe-row-align", type=int, default=256, choices=[128, 256],
                     help="expert segment alignment of the MoE layout (256: one pair tile per slot)")
     return ap.parse_args()
@@ -486,6 +488,8 @@ def run_ours(args, rank, world, local_rank):
         if st != 0:
             raise RuntimeError(f"device status {where}: {ops.STATUS_NAMES.get(st)}")
 
+    if args.sections_only:
+        return run_sections(args, torch, ops, W, dev, stream, tm, fp4_burst, hbm_gbs, check_status, world)
     # ------------------------------------------------------------------ headline
     wl = W.config5()
     x5 = bf16_dev(torch, wl.x, dev)
@@ -652,24 +656,37 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
 
-    secs = [s for s in args.sections.split(",") if s and s != "none"]
-    if "c4" in secs:
-        result["heavy_tail_16384x4096x4096"], n = section_c4(torch, ops, W, dev, tm, args, fp4_burst, hbm_gbs)
-        launches += n
-    if "c2" in secs:
-        result["qwen3_4b_up_proj_4096x9728x2560"], n = section_c2(torch, ops, W, dev, stream, tm, args,
-                                                                  fp4_burst, hbm_gbs)
-        launches += n
-    if "c3" in secs:
-        result["qwen3_30b_a3b_moe_4096tok"], n = section_c3(torch, ops, W, dev, stream, tm, args, hbm_gbs)
-        launches += n
-    check_status("after the run")
+    sections = run_sections(args, torch, ops, W, dev, stream, tm, fp4_burst, hbm_gbs, check_status, world)
+    launches += sections.pop("gpu_launches")
+    result.update(sections)
     result["gpu_launches"] = launches
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline()
     if world > 1:
         torch.distributed.destroy_process_group()
     return result
+
+
+def run_sections(args, torch, ops, W, dev, stream, tm, fp4_burst, hbm_gbs, check_status, world):
+    """The extra workloads (per call): heavy-tailed, Qwen3-4B learner layer,
+    MoE step at 4096 tokens."""
+    out, launches = {}, 0
+    secs = [s for s in args.sections.split(",") if s and s != "none"]
+    if "c4" in secs:
+        out["heavy_tail_16384x4096x4096"], n = section_c4(torch, ops, W, dev, tm, args, fp4_burst, hbm_gbs)
+        launches += n
+    if "c2" in secs:
+        out["qwen3_4b_up_proj_4096x9728x2560"], n = section_c2(torch, ops, W, dev, stream, tm, args, fp4_burst,
+                                                               hbm_gbs)
+        launches += n
+    if "c3" in secs:
+        out["qwen3_30b_a3b_moe_4096tok"], n = section_c3(torch, ops, W, dev, stream, tm, args, hbm_gbs)
+        launches += n
+    check_status("after the sections")
+    out["gpu_launches"] = launches
+    if args.sections_only and world > 1:
+        torch.distributed.destroy_process_group()
+    return out
 
 
 def run_e2e(args, torch, ops, dev, stream, wl, dense, moe, world):

@@ -533,6 +533,24 @@ NVFP4_API nvfp4_status nvfp4_debug_cvt_probe(uint32_t* first, uint32_t* last, ui
  */
 NVFP4_API nvfp4_status nvfp4_debug_wait_timeout(int64_t timeout_ns, nvfp4_stream_t stream);
 
+/*
+ * Failure-detection check of the GEMMs' abort path: every wait of the GEMM
+ * pipelines launched after this call (until it is called again) gives up after
+ * limit_ns instead of the default 2 s; 0 restores the default (0 .. 10 s).
+ * Limits are enforced at the resolution of the GPU's global timer (so a limit
+ * of a few microseconds may outlast every wait); with 1 ns, every wait that is
+ * not complete at its first attempt gives up: the role that gave up records
+ * NVFP4_ERR_TIMEOUT and raises the CTA's abort flag, every
+ * role of both CTAs of a pair leaves its loop, copies and tensor-core work in
+ * flight complete, TMEM is freed and the kernel returns, leaving the context
+ * usable (the output is then incomplete).  Process-wide; not for use while
+ * other threads launch GEMMs.  The GEMMs run a separate build of their kernels
+ * while a limit other than the default is set (the default build keeps the
+ * default limit as a constant); nvfp4_grouped_gemm_swiglu then returns
+ * NVFP4_ERR_INVALID_ARG.
+ */
+NVFP4_API nvfp4_status nvfp4_debug_set_gemm_wait_limit(int64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

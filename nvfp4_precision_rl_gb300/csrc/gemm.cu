@@ -49,6 +49,8 @@
 // nothing in flight.)
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "swiglu.cuh"
 
@@ -94,8 +96,8 @@ struct EpiInfo {
 constexpr int kInfoSlots = 2;
 constexpr uint32_t kSBBytes = kInfoSlots * sizeof(EpiInfo) > kEpiWarps * (kBN / 2) * 4
                                   ? kInfoSlots * sizeof(EpiInfo) : kEpiWarps * (kBN / 2) * 4;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
-constexpr uint64_t kDrainLimitNs = 200000000ull;      // 0.2 s
+constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s: the default pipeline wait limit
+constexpr uint64_t kDrainLimitNs = 50000000ull;       // 50 ms
 
 struct GemmParams {
     const uint8_t* sfa;
@@ -125,6 +127,7 @@ struct GemmParams {
     int64_t ffn;              // swiglu: F (= N, the output columns)
     int64_t b_rows;           // rows of B per expert: N, or 2F with swiglu
     int n_step;               // output columns per tile: 256, or 128 with swiglu
+    uint64_t wait_limit_ns;   // every pipeline wait gives up after this long
 };
 
 // ----------------------------------------------------------------------------
@@ -358,6 +361,27 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
+// The same wait for short (debug) limits, as mbar_wait_short.
+__device__ __forceinline__ bool mbar_wait_cluster_short(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                        volatile int* abort) {
+    const uint32_t hint = static_cast<uint32_t>(limit_ns / 10 + 1);
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_cluster_hint(bar, parity, hint)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+        if (abort != nullptr && *abort) return false;
+    }
+}
+
 // Bounded wait with cluster-scope acquire (the arrivals come from the peer CTA).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int* abort) {
@@ -477,7 +501,7 @@ __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int
     return tl;
 }
 
-template <bool kGrouped, bool kSwiGLU>
+template <bool kGrouped, bool kSwiGLU, bool kShortWaits>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                            const __grid_constant__ CUtensorMap tma_b,
@@ -545,6 +569,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     pdl_wait();             // the producers of the operands and offsets have completed
+    // Pipeline waits: the 2 s default, or the debug limit of the short-wait
+    // instantiation (nvfp4_debug_set_gemm_wait_limit).
+    auto wait_c = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return kShortWaits ? mbar_wait_cluster_short(bar, parity, p.wait_limit_ns, abort_flag)
+                           : mbar_wait_cluster(bar, parity, kWaitLimitNs, abort_flag);
+    };
+    auto wait_b = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return kShortWaits ? mbar_wait_short(bar, parity, p.wait_limit_ns, abort_flag)
+                           : mbar_wait_bounded(bar, parity, kWaitLimitNs, abort_flag);
+    };
     int tiles = num_pm * p.num_n_tiles;
     int mrows = 128;   // grouped: rows per slot of the padded layout
     int64_t used = p.M;   // grouped: rows of the layout in use (offsets[E])
@@ -601,7 +635,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     ok = __all_sync(kPLoadMask,
-                                    mbar_wait_cluster(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag));
+                                    wait_c(&empty[stage], phase ^ 1u));
                     if (!ok) break;
                     const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
                     const uint32_t sf_bytes = ng * kSFAtomBytes;
@@ -659,13 +693,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const uint64_t b_desc0 = sw128_desc(sB);
             for (int t = pair; t < tiles && ok; t += npairs) {
                 if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows).run) continue;
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(acc_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag));
+                ok = __all_sync(0xFFFFFFFFu, wait_c(acc_empty, acc_phase ^ 1u));
                 if (!ok) break;
                 tc_fence_after();
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     // both CTAs' scale warps have seen their stage full and written TMEM
                     ok = __all_sync(0xFFFFFFFFu,
-                                    mbar_wait_cluster(&sf_ready[stage], phase, kWaitLimitNs, abort_flag));
+                                    wait_c(&sf_ready[stage], phase));
                     if (!ok) break;
                     tc_fence_after();
                     const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
@@ -739,7 +773,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                         b[i] = (n < p.N) ? __ldg(sbp + c * p.sb_stride) : 0.0f;
                     }
                 }
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&info_empty[slot], phase ^ 1u, kWaitLimitNs, abort_flag));
+                ok = __all_sync(0xFFFFFFFFu, wait_b(&info_empty[slot], phase ^ 1u));
                 if (!ok) break;
                 EpiInfo* e = info + slot;
     #pragma unroll
@@ -762,7 +796,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
             if (ok) {
                 // the end marker, once its slot is free
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&info_empty[slot], phase ^ 1u, kWaitLimitNs, abort_flag));
+                ok = __all_sync(0xFFFFFFFFu, wait_b(&info_empty[slot], phase ^ 1u));
                 if (ok && lane == 0) {
                     info[slot].end = 1;
                     mbar_arrive(&info_full[slot]);
@@ -783,7 +817,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             for (int t = pair; t < tiles && ok; t += npairs) {
                 if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows).run) continue;
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
-                    bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
+                    bool got = wait_b(&full[stage], phase);
                     got = __all_sync(0xFFFFFFFFu, got);
                     if (!got) {
                         ok = false;
@@ -852,7 +886,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 const float* sb_s;
                 if constexpr (kGrouped) {
                     // the next tile's origin and scales, from the scheduler warp
-                    bool got = mbar_wait_bounded(&info_full[islot], iphase, kWaitLimitNs, abort_flag);
+                    bool got = wait_b(&info_full[islot], iphase);
                     got = __all_sync(0xFFFFFFFFu, got);
                     if (!got) {
                         *abort_flag = 1;
@@ -886,7 +920,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                     __syncwarp();
                     sb_s = sb_w;
                 }
-                bool ok = mbar_wait_cluster(acc_full, acc_phase, kWaitLimitNs, abort_flag);
+                bool ok = wait_c(acc_full, acc_phase);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) {
                     *abort_flag = 1;
@@ -1013,23 +1047,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 // ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(ptr);
-    }();
-    return fn;
-}
+using EncodeTiledFn = TensorMapEncodeTiledFn;
+EncodeTiledFn encode_fn() { return tensor_map_encode_fn(); }
 
 // Rows of `row_bytes` packed bytes; box = 128 bytes x box_rows, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
@@ -1057,12 +1076,12 @@ bool make_map_y(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGrouped, bool kSwiGLU>
+template <bool kGrouped, bool kSwiGLU, bool kShortWaits>
 nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
                               const GemmParams& p, int64_t pair_tiles, const DeviceCtx& ctx, cudaStream_t s) {
     static unsigned long long attr_set[64] = {};   // per context: see ctx_cached
     if (!ctx_cached(attr_set, ctx)) {
-        if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU, kShortWaits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kPSmemBytes)) != cudaSuccess)
             return NVFP4_ERR_CUDA;
         ctx_cache_set(attr_set, ctx);
@@ -1076,7 +1095,7 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
         cfg.blockDim = dim3(kPThreads, 1, 1);
         cfg.dynamicSmemBytes = kPSmemBytes;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU>, &cfg) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU, kShortWaits>, &cfg) != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
             n = ctx.sm_count / 2;
         }
@@ -1097,10 +1116,14 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU>, ma, mb, my, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU, kShortWaits>, ma, mb, my, p) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return NVFP4_OK;
 }
+
+// Pipeline wait limit of the next GEMM launches: the default, or a short limit
+// set through nvfp4_debug_set_gemm_wait_limit to exercise the abort path.
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 
 nvfp4_status check_operand_shapes(int64_t N, int64_t K) {
     if (N <= 0 || N % 16 != 0 || K <= 0 || K % 64 != 0) return NVFP4_ERR_SHAPE;
@@ -1155,13 +1178,16 @@ nvfp4_status nvfp4_gemm_ex(const void* a_q, const void* a_sf, const float* a_s, 
     p.sa_stride = a_s_per_row ? 1 : 0;
     p.sb_stride = b_s_per_row ? 1 : 0;
     p.n_fast = N < M ? 1 : 0;
+    p.wait_limit_ns = g_wait_limit_ns.load();
     p.swiglu = 0;
     p.ffn = 0;
     p.b_rows = N;
     p.n_step = kBN;
     const int64_t pair_tiles = ceil_div(M, 256) * p.num_n_tiles;
     if (pair_tiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
-    return launch_gemm_pair<false, false>(ma, mb, my, p, pair_tiles, ctx, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return p.wait_limit_ns == kWaitLimitNs ? launch_gemm_pair<false, false, false>(ma, mb, my, p, pair_tiles, ctx, s)
+                                           : launch_gemm_pair<false, false, true>(ma, mb, my, p, pair_tiles, ctx, s);
 }
 
 nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int64_t M,
@@ -1220,14 +1246,18 @@ nvfp4_status grouped_gemm(const void* a_q, const void* a_sf, const float* a_s, i
     p.sa_stride = 1;
     p.sb_stride = 1;
     p.n_fast = 0;
+    p.wait_limit_ns = g_wait_limit_ns.load();
     p.swiglu = swiglu ? 1 : 0;
     p.ffn = swiglu ? N : 0;
     p.b_rows = b_rows;
     // slots: every 128-row tile of the capacity x every n-tile (about half start a pair tile)
     const int64_t slots = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     if (slots > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
-    return swiglu ? launch_gemm_pair<true, true>(ma, mb, my, p, (slots + 1) / 2, ctx, stream)
-                  : launch_gemm_pair<true, false>(ma, mb, my, p, (slots + 1) / 2, ctx, stream);
+    const int64_t pair_tiles = (slots + 1) / 2;
+    if (p.wait_limit_ns != kWaitLimitNs)   // debug: short pipeline waits (not for the SwiGLU epilogue)
+        return swiglu ? NVFP4_ERR_INVALID_ARG : launch_gemm_pair<true, false, true>(ma, mb, my, p, pair_tiles, ctx, stream);
+    return swiglu ? launch_gemm_pair<true, true, false>(ma, mb, my, p, pair_tiles, ctx, stream)
+                  : launch_gemm_pair<true, false, false>(ma, mb, my, p, pair_tiles, ctx, stream);
 }
 
 }  // namespace
@@ -1249,6 +1279,12 @@ nvfp4_status nvfp4_grouped_gemm_swiglu(const void* a_q, const void* a_sf, const 
                                        int64_t K, void* h, nvfp4_stream_t stream) {
     return grouped_gemm(a_q, a_sf, a_s, rows_capacity, expert_offsets, E, b_q, b_sf, b_s, ffn, K, h, true,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_debug_set_gemm_wait_limit(int64_t limit_ns) {
+    if (limit_ns < 0 || limit_ns > 10000000000LL) return NVFP4_ERR_INVALID_ARG;
+    g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : static_cast<uint64_t>(limit_ns));
+    return NVFP4_OK;
 }
 
 }  // extern "C"

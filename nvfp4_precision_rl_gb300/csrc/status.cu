@@ -81,6 +81,19 @@ nvfp4_status device_ctx(DeviceCtx* ctx) {
     return g_ctx_state[dev];
 }
 
+TensorMapEncodeTiledFn tensor_map_encode_fn() {
+    static const TensorMapEncodeTiledFn fn = []() -> TensorMapEncodeTiledFn {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<TensorMapEncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
 // ---------------------------------------------------------------------------
 // Exhaustive conversion probe
 // ---------------------------------------------------------------------------

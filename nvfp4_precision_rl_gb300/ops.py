@@ -73,6 +73,7 @@ def lib():
         "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "nvfp4_debug_cvt_probe": (st, [P, P, P, P]),
         "nvfp4_debug_wait_timeout": (st, [I64, P]),
+        "nvfp4_debug_set_gemm_wait_limit": (st, [I64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -231,6 +232,10 @@ def nvfp4_debug_cvt_probe(first, last, counters, stream=None):
 
 def nvfp4_debug_wait_timeout(timeout_ns, stream=None):
     _ok("nvfp4_debug_wait_timeout", lib().nvfp4_debug_wait_timeout(timeout_ns, _s(stream)))
+
+
+def nvfp4_debug_set_gemm_wait_limit(limit_ns):
+    _ok("nvfp4_debug_set_gemm_wait_limit", lib().nvfp4_debug_set_gemm_wait_limit(limit_ns))
 
 
 # ---------------------------------------------------------------------------

@@ -137,3 +137,50 @@ def test_config4_sampled(nv, orc):
 def test_config5_sampled(nv, orc):
     wl = W.config5(moe=False)
     _run(nv, orc, wl.x, wl.w, "config5", sample=_sample(np.random.default_rng(6), 65536, 6144))
+
+
+def test_gemm_abort_path_records_timeout_and_context_stays_usable(nv):
+    """With the GEMM pipeline wait limit set to 1 ns (every wait that is not
+    complete at its first attempt gives up; the limit is enforced at the
+    resolution of the GPU's global timer), a dense and a grouped GEMM each
+    record NVFP4_ERR_TIMEOUT and return: every role of both CTAs leaves its
+    loop, copies and MMAs in flight complete, TMEM is freed.  With the default
+    limit restored, the same GEMMs in the same context give the same bytes as
+    before into freshly poisoned outputs."""
+    import time
+    x = torch.randn(4096, 2560, device="cuda").to(torch.bfloat16)
+    w = (torch.randn(9728, 2560, device="cuda") * 0.02).to(torch.bfloat16)
+    a, b = nv.quantize(x), nv.quantize(w)
+    T, H, N, E, k = 2048, 1024, 512, 16, 4
+    ids = torch.from_numpy(W.route_topk(np.random.default_rng(5), T, E, k)).cuda()
+    perm = nv.moe_permute(ids, E, row_align=256)
+    ga = nv.quantize(torch.randn(T, H, device="cuda").to(torch.bfloat16), gather=perm["gather"])
+    gw = nv.quantize_experts((torch.randn(E, N, H, device="cuda") * 0.02).to(torch.bfloat16))
+    y = torch.empty(4096, 9728, dtype=torch.bfloat16, device="cuda")
+    yg = torch.empty(ga["rows"], N, dtype=torch.bfloat16, device="cuda")
+
+    def run():
+        y.view(torch.int16).fill_(0x7FC1)          # NaN: nothing left over from an earlier call
+        yg.view(torch.int16).fill_(0x7FC1)
+        nv.gemm(a, b, out=y)
+        nv.grouped_gemm(ga, perm["offsets"], E, gw["q"], gw["sf"], gw["s"], N, H, out=yg)
+        torch.cuda.synchronize()
+    run()
+    assert nv.nvfp4_get_device_status() == 0
+    used = int(perm["offsets"][E].item())
+    ref, refg = y.clone(), yg[:used].clone()
+    statuses = []
+    try:
+        nv.nvfp4_debug_set_gemm_wait_limit(1)
+        for fn in (lambda: nv.gemm(a, b, out=y),
+                   lambda: nv.grouped_gemm(ga, perm["offsets"], E, gw["q"], gw["sf"], gw["s"], N, H, out=yg)):
+            t0 = time.time()
+            fn()
+            torch.cuda.synchronize()
+            statuses.append((nv.nvfp4_get_device_status(), time.time() - t0 < 5.0))
+    finally:
+        nv.nvfp4_debug_set_gemm_wait_limit(0)
+    assert statuses == [(6, True), (6, True)], statuses    # NVFP4_ERR_TIMEOUT, returned promptly
+    run()
+    assert nv.nvfp4_get_device_status() == 0
+    assert torch.equal(y, ref) and torch.equal(yg[:used], refg)
