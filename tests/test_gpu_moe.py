@@ -88,8 +88,11 @@ def test_swiglu_quantize(nv, orc, R, F):
     # rows whose h agrees exactly quantize bit-exactly; the fused quantize is
     # the row quantizer's own code, checked against the GPU row quantizer too
     ref = orc.quantize(h_ref)
-    same = np.all(host(got["h"]).view(np.uint16) == h_ref, axis=1)
-    assert same.mean() > 0.5
+    hb = host(got["h"]).view(np.uint16)
+    same = np.all(hb == h_ref, axis=1)
+    # measured: about 1e-5 of h values one ulp from the correctly rounded one
+    # (the binary32 silu's error straddling a bf16 rounding midpoint)
+    assert np.mean(hb != h_ref) < 1e-4 and same.mean() > 0.9
     assert_quant_equal(got, ref, rows=np.nonzero(same)[0], what="swiglu rows")
     again = nv.quantize(got["h"])
     assert torch.equal(again["q"], got["q"]) and torch.equal(again["sf"], got["sf"])

@@ -176,7 +176,7 @@ def test_swiglu_quantize_rollout(nv, orc, rollout):
     same = np.all(hb == h_ref, axis=1)
     print(f"swiglu rollout: {same.mean():.4f} of sampled rows with h bit-exact, "
           f"{np.mean(hb != h_ref):.2e} of elements one ulp apart")
-    assert same.mean() > 0.5
+    assert np.mean(hb != h_ref) < 1e-4 and same.mean() > 0.95
     ref = orc.quantize(h_ref)
     sel = torch.from_numpy(rows[same]).cuda()
     assert np.array_equal(host(got["q"][sel]), ref["q"][same])
