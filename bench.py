@@ -22,10 +22,11 @@ value    = algorithmic GEMM FLOP of the step (2 M N K dense + 2 R (2F H + F H)
 e2e      = the same metric through the library calls with HOST buffers: the
            step's inputs copied in from pinned memory and both outputs copied
            back inside the timed region.
-roofline = the kernel that takes most of the step (the grouped GEMM): its
-           algorithmic FLOP over its launches' CUDA-event durations inside the
-           timed region, against the FP4 peak derived from the measured bf16
-           peak (x6, the 13.5/2.25 nominal ratio); fraction of 9 PF beside it.
+roofline = the kernel that takes most of the step (the grouped GEMM with the
+           SwiGLU epilogue, fc1): its algorithmic FLOP over its CUDA-event
+           duration inside the timed region, against the FP4 peak derived from
+           the measured bf16 peak (x6, the 13.5/2.25 nominal ratio); fraction
+           of 9 PF beside it.
 Sections: the dense GEMM and the quantizer of the same workload per call, the
 heavy-tailed 16384x4096x4096 workload (per-token and per-tensor), the Qwen3-4B
 learner layer (column copy, backward GEMMs, dequantize, MXFP8) and the MoE
@@ -264,7 +265,7 @@ class DenseLayer:
     def stages(self):
         return [Stage("quantize_x_w", self.quantize, 2 if self.column_copy else 1, nbytes=self.quant_bytes(),
                       kernel="quant_rows_staged_kernel"),
-                Stage("gemm", self.gemm, 1, flop=self.flop(), kernel="nvfp4_gemm_pair_kernel<0>")]
+                Stage("gemm", self.gemm, 1, flop=self.flop(), kernel="nvfp4_gemm_pair_kernel<0, 0, 0>")]
 
 
 class MoELayer:
@@ -345,7 +346,7 @@ class MoELayer:
         return [
             Stage("permute", lambda: o.nvfp4_moe_permute(ids, T, k, E, al, self.off, self.gather, cap, self.dst,
                                                          self.pws, self.pws_b, s), 3, nbytes=nb["permute"],
-                  kernel="perm_*"),
+                  kernel="perm_count/scan/scatter_kernel"),
             # per-token quantization of the tokens once, then their rows copied to the
             # routed layout (equal, bit for bit, to quantizing the gathered rows)
             Stage("quantize_tokens", lambda: o.nvfp4_quantize_per_token(
@@ -359,14 +360,14 @@ class MoELayer:
             Stage("grouped_fc1_swiglu", lambda: o.nvfp4_grouped_gemm_swiglu(
                 self.a["q"], self.a["sf"], self.a["s"], cap, self.off, E, self.w1["q"], self.w1["sf"],
                 self.w1["s"], F, H, self.h, s), 1, flop=fl1, nbytes=nb["grouped_fc1_swiglu"],
-                kernel="nvfp4_gemm_pair_kernel<1>"),
+                kernel="nvfp4_gemm_pair_kernel<1, 1, 0>"),
             Stage("quantize_h", lambda: o.nvfp4_quantize_per_token(
                 self.h, cap, F, F, None, cap, o.PER_TOKEN, self.hq["q"], self.hq["sf"], self.hq["s"], stream=s), 1,
-                nbytes=nb["quantize_h"], kernel="quant_rows_staged_kernel"),
+                nbytes=nb["quantize_h"], kernel="quant_rows_staged_kernel (768 columns)"),
             Stage("grouped_fc2", lambda: o.nvfp4_grouped_gemm(
                 self.hq["q"], self.hq["sf"], self.hq["s"], cap, self.off, E, self.w2["q"], self.w2["sf"],
                 self.w2["s"], H, F, self.y2, s), 1, flop=fl2, nbytes=nb["grouped_fc2"],
-                kernel="nvfp4_gemm_pair_kernel<1>"),
+                kernel="nvfp4_gemm_pair_kernel<1, 0, 0>"),
             Stage("combine", lambda: o.nvfp4_moe_combine(self.y2, cap, H, self.dst, self.cw, T, k, H, out, H, s),
                   1, nbytes=nb["combine"], kernel="combine_kernel"),
         ]
