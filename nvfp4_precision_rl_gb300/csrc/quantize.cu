@@ -245,6 +245,163 @@ __global__ void __launch_bounds__(512, staged_ctas_per_sm<NB>()) quant_rows_stag
 }
 
 // Rows longer than 256 * 16 elements: two passes over the row (the second from L1/L2).
+// Narrow rows (up to 64 blocks = 1024 columns): each warp quantizes TWO rows
+// per step, so a step's 2 x nblocks blocks fill whole lane rounds (768
+// columns: 96 blocks = three rounds of 32 instead of 1.5 rounds per row with
+// a quarter of the lanes idle) and the per-row work (the wait, the copy issue,
+// the amax reduction, the outer scale) is shared by two rows.  Row pairs
+// (2k, 2k+1) of the job's row slots are walked grid-stride per warp; a pair
+// sits in one staging slot (both rows copied by bulk TMA, one mbarrier).  The
+// per-block arithmetic is the one-row kernel's (rowquant.cuh): same bytes.
+template <int NU, int MODE>
+__global__ void __launch_bounds__(512, 2) quant_row_pairs_kernel(RowJob job, StageCfg cfg) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_launch_dependents();    // a dependent waits for this grid's completion itself
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const uint32_t slot_bytes = 2 * cfg.row_pad;
+    uint8_t* bufs = smem + static_cast<size_t>(warp) * cfg.depth * slot_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(nwarps) * cfg.depth * slot_bytes) +
+                     warp * cfg.depth;
+    const int nblocks = job.t0.cols >> 4;
+    const int kgroups = job.t0.kgroups;
+    const uint32_t row_bytes = static_cast<uint32_t>(job.t0.cols) * 2u;
+    const float tensor_amax = (MODE == kPerTensor) ? __uint_as_float(*job.t0.amax_ws) : 0.0f;
+    const int64_t pairs = (job.total + 1) >> 1;   // a last odd slot (amax-only pass) pairs with a pad row
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * nwarps;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+
+    if (lane == 0) {
+        for (int d = 0; d < cfg.depth; ++d) mbar_init(&bars[d], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // source row of row slot r (-1: a pad row past rows_out, or a dropped gather index)
+    auto source = [&](int64_t r) -> int64_t {
+        const bool sec = r >= job.split;
+        const RowParams& t = sec ? job.t1 : job.t0;
+        const int64_t lr = sec ? r - job.split : r;
+        if (lr >= t.rows_out) return -1;
+        int64_t src = t.gather ? static_cast<int64_t>(t.gather[lr]) : lr;
+        if (src >= t.rows_in) {
+            record_error(job.t0.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
+            src = -1;
+        }
+        return src;
+    };
+    // lane 0: copy pair k's rows with a source into slot d (one arrival; bytes as copied)
+    auto issue = [&](int64_t k, int d) {
+        if (k >= pairs || lane != 0) return;
+        const int64_t s0 = source(2 * k), s1 = source(2 * k + 1);
+        const bool sec = 2 * k >= job.split;
+        const uint16_t* x = sec ? job.t1.x : job.t0.x;
+        const int64_t ld = sec ? job.t1.ld_x : job.t0.ld_x;
+        mbar_arrive_expect_tx(&bars[d], (s0 >= 0 ? row_bytes : 0u) + (s1 >= 0 ? row_bytes : 0u));
+        uint8_t* dst = bufs + static_cast<size_t>(d) * slot_bytes;
+        if (s0 >= 0) bulk_row_load(dst, x + s0 * ld, row_bytes, &bars[d]);
+        if (s1 >= 0) bulk_row_load(dst + cfg.row_pad, x + s1 * ld, row_bytes, &bars[d]);
+    };
+    for (int d = 0; d < cfg.depth; ++d) issue(first + d * stride, d);
+
+    float seen0 = 0.0f, seen1 = 0.0f;
+    uint32_t parity = 0;
+    int d = 0;
+    for (int64_t k = first; k < pairs; k += stride) {
+        const int64_t r0 = 2 * k;
+        const bool sec = r0 >= job.split;
+        const RowParams& t = sec ? job.t1 : job.t0;
+        const int64_t lr0 = sec ? r0 - job.split : r0;
+        // per row of the pair: pad (past rows_out: only its scale words are
+        // written, as zeros) or zero (no source: encodes as a zero row)
+        auto no_source = [&](int64_t lr) {
+            if (lr >= t.rows_out) return true;
+            const int64_t src = t.gather ? static_cast<int64_t>(t.gather[lr]) : lr;
+            return src < 0 || src >= t.rows_in;
+        };
+        const bool pad0 = lr0 >= t.rows_out, pad1 = lr0 + 1 >= t.rows_out;
+        const bool zero0 = no_source(lr0), zero1 = no_source(lr0 + 1);
+        bool ok = mbar_wait_bounded(&bars[d], (parity >> d) & 1u, 2000000000ull, nullptr);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                record_error(job.t0.status, NVFP4_ERR_TIMEOUT, DETAIL_NONE);
+                for (int j = 0; j < cfg.depth; ++j) {
+                    const int bb = (d + j) % cfg.depth;
+                    if (k + j * stride < pairs) mbar_wait_bounded(&bars[bb], (parity >> bb) & 1u, 200000000ull, nullptr);
+                }
+            }
+            break;
+        }
+        parity ^= 1u << d;
+        const uint8_t* slot = bufs + static_cast<size_t>(d) * slot_bytes;
+        // unit u = i * 32 + lane: row u / nblocks, block u % nblocks
+        Block16 v[NU];
+        int hrow[NU], blk[NU];
+#pragma unroll
+        for (int i = 0; i < NU; ++i) {
+            const int u = i * 32 + lane;
+            hrow[i] = u >= nblocks ? 1 : 0;
+            blk[i] = u - hrow[i] * nblocks;
+            const bool in = u < 2 * nblocks && !(hrow[i] ? zero1 : zero0);
+            const uint4* row = reinterpret_cast<const uint4*>(slot + hrow[i] * cfg.row_pad);
+            v[i].lo = in ? row[2 * blk[i]] : make_uint4(0u, 0u, 0u, 0u);
+            v[i].hi = in ? row[2 * blk[i] + 1] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();                       // every lane has read the slot
+        issue(k + cfg.depth * stride, d);   // refill it with the pair `depth` steps ahead
+        d = (d + 1 == cfg.depth) ? 0 : d + 1;
+        float bmax[NU];
+        float am0 = 0.0f, am1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NU; ++i) {
+            bmax[i] = block_absmax(v[i]);
+            if (hrow[i]) am1 = fmaxf(am1, bmax[i]);
+            else am0 = fmaxf(am0, bmax[i]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            am0 = fmaxf(am0, __shfl_xor_sync(0xFFFFFFFFu, am0, o));
+            am1 = fmaxf(am1, __shfl_xor_sync(0xFFFFFFFFu, am1, o));
+        }
+        if (sec) seen1 = fmaxf(seen1, fmaxf(am0, am1));
+        else seen0 = fmaxf(seen0, fmaxf(am0, am1));
+        if (MODE == kAmaxOnly) continue;
+        const ScaleRecipe rec0(MODE == kPerTensor ? tensor_amax : am0);
+        const ScaleRecipe rec1(MODE == kPerTensor ? tensor_amax : am1);
+        uint2* q = reinterpret_cast<uint2*>(t.q);
+#pragma unroll
+        for (int i = 0; i < NU; ++i) {
+            const int u = i * 32 + lane;
+            const int h = hrow[i];
+            const int64_t lr = lr0 + h;
+            const int b = blk[i];
+            if (u >= 2 * nblocks) continue;
+            if (h ? pad1 : pad0) {
+                // a pad row's scale words are zero (blocks 4g.. of its row, one byte each)
+                if ((b >> 2) < kgroups) t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = 0;
+                continue;
+            }
+            float rb;
+            const uint32_t sb = (h ? rec1 : rec0).block(bmax[i], &rb);
+            const float2 r2 = make_float2(rb, rb);
+            q[lr * nblocks + b] = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
+            t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
+        }
+        // the padding of a row's last scale word (blocks nblocks .. 4 kgroups) is zero
+        if (lane < 2 && (nblocks & 3) != 0) {
+            const int64_t lr = lr0 + lane;
+            for (int b = nblocks; b < 4 * kgroups; ++b) t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = 0;
+        }
+        if (lane < 2 && !(lane ? pad1 : pad0)) t.s[lr0 + lane] = (lane ? rec1 : rec0).S;
+    }
+    if (MODE != kPerTensor && lane == 0) {
+        if (job.t0.amax_ws != nullptr && seen0 > 0.0f) atomicMax(job.t0.amax_ws, __float_as_uint(seen0));
+        if (job.t1.amax_ws != nullptr && seen1 > 0.0f) atomicMax(job.t1.amax_ws, __float_as_uint(seen1));
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kRowThreads) quant_rows_long_kernel(RowParams p) {
     pdl_launch_dependents();    // a dependent waits for this grid's completion itself
@@ -455,10 +612,42 @@ nvfp4_status launch_staged(const RowJob& job, int warps, StageCfg cfg, const Dev
     return NVFP4_OK;
 }
 
+template <int NU, int MODE>
+nvfp4_status launch_row_pairs(const RowJob& job, const DeviceCtx& ctx, cudaStream_t s) {
+    constexpr int kWarps = 16;
+    StageCfg cfg;
+    cfg.depth = 2;
+    cfg.row_pad = static_cast<uint32_t>(round_up(static_cast<int64_t>(job.t0.cols) * 2, 128));
+    const size_t smem = static_cast<size_t>(kWarps) * cfg.depth * (2 * cfg.row_pad + 8);
+    static unsigned long long attr[64] = {};   // per context: see ctx_cached
+    if (!ctx_cached(attr, ctx)) {
+        if (cudaFuncSetAttribute(quant_row_pairs_kernel<NU, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 210 * 1024) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        ctx_cache_set(attr, ctx);
+    }
+    const int64_t want = ceil_div((job.total + 1) / 2, kWarps);
+    const int64_t cap = static_cast<int64_t>(ctx.sm_count) * (2 * smem <= 220 * 1024 ? 2 : 1);
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    quant_row_pairs_kernel<NU, MODE><<<grid, kWarps * 32, smem, s>>>(job, cfg);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
+}
+
 // Staged path for a job (one or two tensors with the same columns); false if
-// the row does not fit the staged geometry (the caller falls back).
+// the row does not fit the staged geometry (the caller falls back).  Rows of
+// up to 64 blocks go two per warp step.
 template <int MODE>
 bool try_launch_staged(const RowJob& job, const DeviceCtx& ctx, cudaStream_t s, nvfp4_status* st) {
+    const int nblocks = job.t0.cols / 16;
+    if (nblocks <= 64) {
+        const int nu = (2 * nblocks + 31) / 32;    // units (blocks of the row pair) per lane
+        if (nu <= 1) *st = launch_row_pairs<1, MODE>(job, ctx, s);
+        else if (nu <= 2) *st = launch_row_pairs<2, MODE>(job, ctx, s);
+        else if (nu <= 3) *st = launch_row_pairs<3, MODE>(job, ctx, s);
+        else *st = launch_row_pairs<4, MODE>(job, ctx, s);
+        return true;
+    }
     int warps = 0;
     StageCfg cfg{0, 0};
     const int nb = (job.t0.cols / 16 + 31) / 32;   // 16-element blocks per lane
