@@ -203,7 +203,10 @@ class Stage:
 
     def __init__(self, name, fn, kernels, flop=0.0, nbytes=0.0, kernel=None):
         self.name, self.fn, self.kernels = name, fn, kernels
-        self.flop, self.nbytes, self.kernel = flop, nbytes, kernel
+        self.flop, self.kernel = flop, kernel
+        # algorithmic bytes: a number, or (read, write)
+        self.rbytes, self.wbytes = nbytes if isinstance(nbytes, tuple) else (nbytes, 0.0)
+        self.nbytes = self.rbytes + self.wbytes
 
 
 def bf16_dev(torch, bits, dev):
@@ -237,15 +240,20 @@ class DenseLayer:
         self.ws = torch.empty(self.wsb, dtype=u8, device=dev)
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
-    def quant_bytes(self):
-        """Algorithmic bytes of the quantize call: read 2 B per element, write
-        0.5 B codes + 1/16 B scales per element + 4 B per row (X and W rows);
-        the column copy writes another 0.5 + 1/16 B per element of X + 4 B."""
+    def quant_rw(self):
+        """Algorithmic (read, write) bytes of the quantize call: read 2 B per
+        element, write 0.5 B codes + 1/16 B scales per element + 4 B per row
+        (X and W rows); the column copy writes another 0.5 + 1/16 B per element
+        of X + 4 B."""
         M, N, K = self.M, self.N, self.K
-        b = (M + N) * K * (2 + 0.5 + 1 / 16) + (M + N) * 4
+        r = (M + N) * K * 2
+        w = (M + N) * K * (0.5 + 1 / 16) + (M + N) * 4
         if self.column_copy:
-            b += M * K * (0.5 + 1 / 16) + 4
-        return b
+            w += M * K * (0.5 + 1 / 16) + 4
+        return r, w
+
+    def quant_bytes(self):
+        return sum(self.quant_rw())
 
     def flop(self):
         return 2.0 * self.M * self.N * self.K
@@ -263,7 +271,7 @@ class DenseLayer:
                             self.qw["s"], self.N, self.K, y, self.N, self.stream)
 
     def stages(self):
-        return [Stage("quantize_x_w", self.quantize, 2 if self.column_copy else 1, nbytes=self.quant_bytes(),
+        return [Stage("quantize_x_w", self.quantize, 2 if self.column_copy else 1, nbytes=self.quant_rw(),
                       kernel="quant_rows_staged_kernel"),
                 Stage("gemm", self.gemm, 1, flop=self.flop(), kernel="nvfp4_gemm_pair_kernel<0, 0, 0>")]
 
@@ -316,23 +324,24 @@ class MoELayer:
         return 2.0 * R * H * 2 * F, 2.0 * R * F * H
 
     def stage_bytes(self):
-        """Algorithmic bytes per stage over the ROUTED rows (padding rows of the
-        aligned layout are not counted): each must move these at least once."""
+        """Algorithmic (read, write) bytes per stage over the ROUTED rows
+        (padding rows of the aligned layout are not counted): each must move
+        these at least once."""
         T, H, F, E, k, R = self.T, self.H, self.F, self.E, self.k, self.routed()
         qrow_h = H // 2 + H // 16 + 4      # codes + block scales + S of one quantized row
         qrow_f = F // 2 + F // 16 + 4
         w1 = E * (2 * F) * (H // 2 + H // 16 + 4)
         w2 = E * H * (F // 2 + F // 16 + 4)
         return {
-            "permute": T * k * 4 + R * 4 + T * k * 4 + (E + 1) * 4,
-            "quantize_tokens": T * H * 2 + T * qrow_h,
+            "permute": (T * k * 4, R * 4 + T * k * 4 + (E + 1) * 4),
+            "quantize_tokens": (T * H * 2, T * qrow_h),
             # each token's quantized row is read once from HBM (its other k - 1
             # reads hit L2) and written to its k routed rows
-            "gather_quantized": T * qrow_h + R * qrow_h,
-            "grouped_fc1_swiglu": R * qrow_h + w1 + R * F * 2,
-            "quantize_h": R * F * 2 + R * qrow_f,
-            "grouped_fc2": R * qrow_f + w2 + R * H * 2,
-            "combine": R * H * 2 + T * k * 8 + T * H * 2,
+            "gather_quantized": (T * qrow_h, R * qrow_h),
+            "grouped_fc1_swiglu": (R * qrow_h + w1, R * F * 2),
+            "quantize_h": (R * F * 2, R * qrow_f),
+            "grouped_fc2": (R * qrow_f + w2, R * H * 2),
+            "combine": (R * H * 2 + T * k * 8, T * H * 2),
         }
 
     def stages(self, x=None, ids=None, out=None):
@@ -452,6 +461,32 @@ class Timer:
             self.torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1) / len(fns))
         return float(np.mean(ts)), len(ts)
+
+
+def one_way_bandwidth(torch, dev, flush):
+    """Read-only and write-only DRAM bandwidth (GB/s) on this GPU, measured with
+    CUDA events: a sum over and a fill of 2 GB (best of five)."""
+    buf = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+    words = buf.view(torch.int64)
+
+    def best(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return buf.numel() / (min(ts) * 1e-3) / 1e9
+    rd = best(lambda: words.sum())
+    wr = best(lambda: buf.fill_(1))
+    del buf, words
+    torch.cuda.empty_cache()
+    return rd, wr
 
 
 def rot_note(n):
@@ -577,6 +612,7 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(ach / hbm_gbs, 4), "traffic": None}
 
     # ---- per-stage rooflines of the step (algorithmic bytes / FLOP over routed rows)
+    rw_bw = one_way_bandwidth(torch, dev, flush)
     stage_report = {}
     for i, st in enumerate(stages):
         ms = float(seg_ms[i])
@@ -584,6 +620,11 @@ def run_ours(args, rank, world, local_rank):
         if st.nbytes:
             r["gbs"] = round(st.nbytes / (ms * 1e-3) / 1e9, 1)
             r["hbm_frac"] = round(st.nbytes / (ms * 1e-3) / 1e9 / hbm_gbs, 4)
+            # DRAM time bound with reads and writes each at their own measured
+            # one-way rate (they share the bus): reads / R + writes / W
+            bound_ms = (st.rbytes / rw_bw[0] + st.wbytes / rw_bw[1]) / 1e9 * 1e3
+            r["rw_bound_ms"] = round(bound_ms, 5)
+            r["frac_of_rw_bound"] = round(bound_ms / ms, 4)
         if st.flop:
             r["tflops"] = round(st.flop / (ms * 1e-3) / 1e12, 1)
             r["frac_of_9pf"] = round(st.flop / (ms * 1e-3) / 1e12 / (PAGES_FP4_PF * 1000), 4)
@@ -642,6 +683,8 @@ def run_ours(args, rank, world, local_rank):
         "kernels_ms": kernels_ms,
         "stages": stage_report,
         "one_graph_ms_per_step": round(float(t_one.mean()), 5),
+        "hbm_one_way_gbs": {"read": round(rw_bw[0], 1), "write": round(rw_bw[1], 1),
+                            "how": "sum over / fill of 2 GB, best of five, CUDA events"},
         "quantize": {"gbs": dense_percall["quantize_x_w"]["gbs"], "frac": dense_percall["quantize_x_w"]["frac"],
                      "hbm_peak_gbs": hbm_gbs, "peak_basis": f"{peak_src} copy bandwidth",
                      "what": "per-token X [65536, 2048] rows + W [6144, 2048] rows, one launch, per call",

@@ -96,6 +96,9 @@ struct EpiInfo {
 constexpr int kInfoSlots = 2;
 constexpr uint32_t kSBBytes = kInfoSlots * sizeof(EpiInfo) > kEpiWarps * (kBN / 2) * 4
                                   ? kInfoSlots * sizeof(EpiInfo) : kEpiWarps * (kBN / 2) * 4;
+// The grouped kernel keeps a copy of the expert offsets in the rest of that space.
+constexpr int kSmemOffsets = static_cast<int>((kSBBytes - kInfoSlots * sizeof(EpiInfo)) / sizeof(int32_t));
+static_assert(kSmemOffsets >= 129, "room for the offsets of 128 experts");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s: the default pipeline wait limit
 constexpr uint64_t kDrainLimitNs = 50000000ull;       // 50 ms
 
@@ -446,7 +449,8 @@ struct PairTile {
 // tiles ends in a tile whose odd CTA reads rows past the expert (its results
 // are computed with this expert's B and never stored).
 template <bool kGrouped, bool kSwiGLU>
-__device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int num_pm, int mrows) {
+__device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int num_pm, int mrows,
+                                                 const int32_t* offs = nullptr) {
     PairTile tl;
     if (!kGrouped) {
         const int mt = p.n_fast ? t / p.num_n_tiles : t % num_pm;
@@ -472,14 +476,14 @@ __device__ __forceinline__ PairTile pair_tile_at(const GemmParams& p, int t, int
     for (int b0 = 0; b0 < nblk; b0 += 8) {
         int v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = (b0 + j < nblk) ? __ldg(p.offsets + 16 * (b0 + j)) : INT_MAX;
+        for (int j = 0; j < 8; ++j) v[j] = (b0 + j < nblk) ? offs[16 * (b0 + j)] : INT_MAX;
 #pragma unroll
         for (int j = 0; j < 8; ++j) cnt += static_cast<int64_t>(v[j]) <= m0;
     }
     const int base = (cnt > 0 ? cnt - 1 : 0) << 4;
     int w[17];
 #pragma unroll
-    for (int j = 0; j < 17; ++j) w[j] = (base + j <= p.E) ? __ldg(p.offsets + base + j) : INT_MAX;
+    for (int j = 0; j < 17; ++j) w[j] = (base + j <= p.E) ? offs[base + j] : INT_MAX;
     int c2 = 0;
 #pragma unroll
     for (int j = 0; j < 16; ++j) c2 += (base + j < p.E && static_cast<int64_t>(w[j]) <= m0);
@@ -520,6 +524,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     uint8_t* sSFB = sSFA + kPStages * kSFATileBytes;
     uint8_t* sOut = sSFB + kPStages * kSFBTileBytes;              // 1024-aligned
     EpiInfo* info = reinterpret_cast<EpiInfo*>(sOut + kPOutBytes);
+    int32_t* s_offsets = reinterpret_cast<int32_t*>(info + kInfoSlots);   // grouped: a copy of the offsets
     uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(info) + kSBBytes);
     uint64_t* empty = full + kPStages;
     uint64_t* sf_ready = empty + kPStages;
@@ -581,15 +586,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     };
     int tiles = num_pm * p.num_n_tiles;
     int mrows = 128;   // grouped: rows per slot of the padded layout
+    const int32_t* offs = p.offsets;   // grouped: where the expert lookups read the offsets
     int64_t used = p.M;   // grouped: rows of the layout in use (offsets[E])
     if (kGrouped) {
         // A layout whose expert segments are all 256-row aligned is walked in
         // 256-row slots, every one a pair tile (the strided assignment then
         // gives every pair the same number of tiles); otherwise in 128-row
         // slots, a pair tile starting at every second one of an expert.
+        // the offsets, copied to shared memory when they fit beside the
+        // tile-information ring: every role's expert lookups then cost
+        // shared-memory latency instead of two rounds of L2 round trips
         bool misaligned = false;
-        for (int e = threadIdx.x; e <= p.E; e += blockDim.x) misaligned |= (__ldg(p.offsets + e) & 255) != 0;
+        for (int e = threadIdx.x; e <= p.E; e += blockDim.x) {
+            const int32_t o = __ldg(p.offsets + e);
+            misaligned |= (o & 255) != 0;
+            if (p.E + 1 <= kSmemOffsets) s_offsets[e] = o;
+        }
         mrows = __syncthreads_or(misaligned) ? 128 : 256;
+        if (p.E + 1 <= kSmemOffsets) offs = s_offsets;
         // slots of the padded layout in use: it ends at offsets[E]
         used = __ldg(p.offsets + p.E);
         if (used > p.M || used < 0) {
@@ -618,9 +632,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                const PairTile tl = pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows);
+                const PairTile tl = pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows, offs);
                 if (!tl.run) continue;
-                if (kGrouped && !side_b && rank == 0 && (__ldg(p.offsets + tl.expert) & 127) != 0)
+                if (kGrouped && !side_b && rank == 0 && (offs[tl.expert] & 127) != 0)
                     record_error(p.status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_OFFSETS);
                 const int64_t m0 = tl.m_base + rank * 128;
                 const int64_t n0 = tl.n0;
@@ -692,7 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             const uint64_t a_desc0 = sw128_desc(sA);
             const uint64_t b_desc0 = sw128_desc(sB);
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows).run) continue;
+                if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows, offs).run) continue;
                 ok = __all_sync(0xFFFFFFFFu, wait_c(acc_empty, acc_phase ^ 1u));
                 if (!ok) break;
                 tc_fence_after();
@@ -750,7 +764,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t slot = 0, phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                const PairTile tl = pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows);
+                const PairTile tl = pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows, offs);
                 if (!tl.run) continue;
                 const int64_t mrow0 = tl.m_base + rank * 128;
                 float a[128 / 32], b[kBN / 32];
@@ -815,7 +829,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows).run) continue;
+                if (mrows != 256 && !pair_tile_at<kGrouped, kSwiGLU>(p, t, num_pm, mrows, offs).run) continue;
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     bool got = wait_b(&full[stage], phase);
                     got = __all_sync(0xFFFFFFFFu, got);
