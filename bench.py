@@ -620,9 +620,10 @@ def run_ours(args, rank, world, local_rank):
         if st.nbytes:
             r["gbs"] = round(st.nbytes / (ms * 1e-3) / 1e9, 1)
             r["hbm_frac"] = round(st.nbytes / (ms * 1e-3) / 1e9 / hbm_gbs, 4)
-            # DRAM time bound with reads and writes each at their own measured
-            # one-way rate (they share the bus): reads / R + writes / W
-            bound_ms = (st.rbytes / rw_bw[0] + st.wbytes / rw_bw[1]) / 1e9 * 1e3
+            # DRAM time bound: the slowest of the reads at the measured read-only
+            # rate, the writes at the write-only rate (~4 TB/s on this part) and
+            # all bytes at the copy rate
+            bound_ms = max(st.rbytes / rw_bw[0], st.wbytes / rw_bw[1], st.nbytes / hbm_gbs) / 1e9 * 1e3
             r["rw_bound_ms"] = round(bound_ms, 5)
             r["frac_of_rw_bound"] = round(bound_ms / ms, 4)
         if st.flop:
