@@ -526,6 +526,23 @@ NVFP4_API nvfp4_status nvfp4_debug_cvt_probe(uint32_t* first, uint32_t* last, ui
                                    nvfp4_stream_t stream);
 
 /*
+ * Self-check of the quantizers' scale arithmetic (block scale code and element
+ * multiplier, "Towards Blackwell-Native 8-bit and 4-bit RL", "Bit-exact
+ * quantizer contract"): rows whose outer scale lies in [2^-90, 2^90] compute the
+ * correctly rounded quotient amax_b / T and reciprocal 1 / D with fused
+ * multiply-adds instead of IEEE division.  This compares the two forms over
+ * every pair of bf16 values the quantizers can meet (row amax, block amax <=
+ * row amax; about 5e8 pairs).
+ *  counters  uint64 [2] (device, 8-byte aligned): [0] pairs compared, [1]
+ *            pairs whose code or multiplier differ (0 when the forms agree).
+ *  mismatch  uint32 [17] (device): [0] mismatches recorded, then up to 8 pairs
+ *            (row amax bits >> 16, block amax bits >> 16).
+ * Both are cleared on the stream first; results are ready when it completes.
+ */
+NVFP4_API nvfp4_status nvfp4_debug_scale_recipe_check(unsigned long long* counters, uint32_t* mismatch,
+                                                      nvfp4_stream_t stream);
+
+/*
  * Failure-detection check: launch one block that waits, with the library's
  * bounded wait, on an mbarrier nothing will ever arrive at.  After timeout_ns
  * (1 ms .. 10 s) the wait gives up, the kernel records NVFP4_ERR_TIMEOUT in the

@@ -371,24 +371,29 @@ __global__ void __launch_bounds__(512, 2) quant_row_pairs_kernel(RowJob job, Sta
         const ScaleRecipe rec0(MODE == kPerTensor ? tensor_amax : am0);
         const ScaleRecipe rec1(MODE == kPerTensor ? tensor_amax : am1);
         uint2* q = reinterpret_cast<uint2*>(t.q);
+        // the FMA form of the scale arithmetic when both rows allow it
+        auto encode = [&](auto form) {
 #pragma unroll
-        for (int i = 0; i < NU; ++i) {
-            const int u = i * 32 + lane;
-            const int h = hrow[i];
-            const int64_t lr = lr0 + h;
-            const int b = blk[i];
-            if (u >= 2 * nblocks) continue;
-            if (h ? pad1 : pad0) {
-                // a pad row's scale words are zero (blocks 4g.. of its row, one byte each)
-                if ((b >> 2) < kgroups) t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = 0;
-                continue;
+            for (int i = 0; i < NU; ++i) {
+                const int u = i * 32 + lane;
+                const int h = hrow[i];
+                const int64_t lr = lr0 + h;
+                const int b = blk[i];
+                if (u >= 2 * nblocks) continue;
+                if (h ? pad1 : pad0) {
+                    // a pad row's scale words are zero (blocks 4g.. of its row, one byte each)
+                    if ((b >> 2) < kgroups) t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = 0;
+                    continue;
+                }
+                float rb;
+                const uint32_t sb = (h ? rec1 : rec0).template block_as<decltype(form)::value>(bmax[i], &rb);
+                const float2 r2 = make_float2(rb, rb);
+                q[lr * nblocks + b] = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
+                t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
             }
-            float rb;
-            const uint32_t sb = (h ? rec1 : rec0).block(bmax[i], &rb);
-            const float2 r2 = make_float2(rb, rb);
-            q[lr * nblocks + b] = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
-            t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
-        }
+        };
+        if (rec0.fast && rec1.fast) encode(std::true_type{});
+        else encode(std::false_type{});
         // the padding of a row's last scale word (blocks nblocks .. 4 kgroups) is zero
         if (lane < 2 && (nblocks & 3) != 0) {
             const int64_t lr = lr0 + lane;

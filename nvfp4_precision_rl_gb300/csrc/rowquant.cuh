@@ -88,15 +88,19 @@ __device__ __forceinline__ void encode_row(const uint4 (&v)[NCH], const float (&
                                            uint8_t* sf, float* s, int64_t r, int lane) {
     const ScaleRecipe rec(amax);
     uint32_t* qrow = q + r * nchunks;
+    auto encode = [&](auto form) {
 #pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-        const int c = i * 32 + lane;
-        float rb;
-        const uint32_t sb = rec.block(bmax[i], &rb);
-        const uint32_t w = encode_chunk(v[i], rb);
-        if (c < nchunks) qrow[c] = w;
-        store_sf_word(sf, kgroups, r, i, lane, sb);
-    }
+        for (int i = 0; i < NCH; ++i) {
+            const int c = i * 32 + lane;
+            float rb;
+            const uint32_t sb = rec.template block_as<decltype(form)::value>(bmax[i], &rb);
+            const uint32_t w = encode_chunk(v[i], rb);
+            if (c < nchunks) qrow[c] = w;
+            store_sf_word(sf, kgroups, r, i, lane, sb);
+        }
+    };
+    if (rec.fast) encode(std::true_type{});
+    else encode(std::false_type{});
     if (lane == 0) s[r] = rec.S;
 }
 
@@ -136,18 +140,22 @@ __device__ __forceinline__ void encode_row_blocks(const Block16 (&v)[NB], const 
                                                   uint8_t* sf, float* s, int64_t r, int lane) {
     const ScaleRecipe rec(amax);
     uint2* qrow = q + r * nblocks;
+    auto encode = [&](auto form) {
 #pragma unroll
-    for (int i = 0; i < NB; ++i) {
-        const int b = i * 32 + lane;
-        float rb;
-        const uint32_t sb = rec.block(bmax[i], &rb);
-        const float2 r2 = make_float2(rb, rb);
-        const uint2 w = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
-        if (b < nblocks) qrow[b] = w;
-        // each lane writes its block's scale byte: four consecutive lanes fill
-        // one swizzled word (blocks past the row's end write zero bytes)
-        if ((b >> 2) < kgroups) sf[sf_word_offset(r, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
-    }
+        for (int i = 0; i < NB; ++i) {
+            const int b = i * 32 + lane;
+            float rb;
+            const uint32_t sb = rec.template block_as<decltype(form)::value>(bmax[i], &rb);
+            const float2 r2 = make_float2(rb, rb);
+            const uint2 w = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
+            if (b < nblocks) qrow[b] = w;
+            // each lane writes its block's scale byte: four consecutive lanes
+            // fill one swizzled word (blocks past the row's end write zero bytes)
+            if ((b >> 2) < kgroups) sf[sf_word_offset(r, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
+        }
+    };
+    if (rec.fast) encode(std::true_type{});
+    else encode(std::false_type{});
     if (lane == 0) s[r] = rec.S;
 }
 

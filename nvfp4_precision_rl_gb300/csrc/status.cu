@@ -168,6 +168,36 @@ __global__ void __launch_bounds__(256) cvt_probe_kernel(uint32_t* first, uint32_
     if (threadIdx.x < 4 && s_cnt[threadIdx.x]) atomicAdd(&counters[threadIdx.x], s_cnt[threadIdx.x]);
 }
 
+// Self-check of the scale recipe's two forms: block i takes the row amax with
+// bf16 bits i (every positive finite bf16 and zero: i = 0 .. 0x7F7F), its threads
+// every block amax a <= amax (bf16 bits j <= i); for a row in the FMA range the
+// FMA form's code and multiplier must equal the IEEE form's, bit for bit.
+// counters[0] = pairs compared (rows in the FMA range), counters[1] = mismatches;
+// mismatch[0] = how many were recorded, then up to 8 (i, j) pairs.
+__global__ void __launch_bounds__(256) recipe_check_kernel(unsigned long long* counters, uint32_t* mismatch) {
+    const uint32_t i = blockIdx.x;
+    const ScaleRecipe rec(__uint_as_float(i << 16));
+    if (!rec.fast) return;
+    unsigned long long n = 0, bad = 0;
+    for (uint32_t j = threadIdx.x; j <= i; j += blockDim.x) {
+        const float a = __uint_as_float(j << 16);
+        float r_fma, r_ieee;
+        const uint32_t s_fma = rec.block_as<true>(a, &r_fma);
+        const uint32_t s_ieee = rec.block_as<false>(a, &r_ieee);
+        ++n;
+        if (s_fma != s_ieee || __float_as_uint(r_fma) != __float_as_uint(r_ieee)) {
+            ++bad;
+            const uint32_t k = atomicAdd(mismatch, 1u);
+            if (k < 8) {
+                mismatch[1 + 2 * k] = i;
+                mismatch[2 + 2 * k] = j;
+            }
+        }
+    }
+    atomicAdd(&counters[0], n);
+    if (bad) atomicAdd(&counters[1], bad);
+}
+
 __global__ void cvt_probe_init_kernel(uint32_t* first, uint32_t* last, uint32_t* counters) {
     for (int i = threadIdx.x; i < 144; i += blockDim.x) {
         first[i] = 0xFFFFFFFFu;
@@ -239,6 +269,22 @@ const char* nvfp4_status_string(nvfp4_status s) {
         case NVFP4_ERR_WORKSPACE: return "NVFP4_ERR_WORKSPACE";
     }
     return "NVFP4_ERR_UNKNOWN";
+}
+
+nvfp4_status nvfp4_debug_scale_recipe_check(unsigned long long* counters, uint32_t* mismatch,
+                                            nvfp4_stream_t stream) {
+    DeviceCtx ctx;
+    nvfp4_status st = device_ctx(&ctx);
+    if (st != NVFP4_OK) return st;
+    if (!counters || !mismatch) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(counters, 8) || !aligned(mismatch, 4)) return NVFP4_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(counters, 0, 2 * sizeof(unsigned long long), s) != cudaSuccess ||
+        cudaMemsetAsync(mismatch, 0, 17 * sizeof(uint32_t), s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    recipe_check_kernel<<<0x7F80, 256, 0, s>>>(counters, mismatch);
+    NVFP4_CHECK_LAUNCH();
+    return NVFP4_OK;
 }
 
 nvfp4_status nvfp4_debug_cvt_probe(uint32_t* first, uint32_t* last, uint32_t* counters,

@@ -72,6 +72,7 @@ def lib():
         "nvfp4_get_device_status": (st, [P]),
         "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "nvfp4_debug_cvt_probe": (st, [P, P, P, P]),
+        "nvfp4_debug_scale_recipe_check": (st, [P, P, P]),
         "nvfp4_debug_wait_timeout": (st, [I64, P]),
         "nvfp4_debug_set_gemm_wait_limit": (st, [I64]),
     }
@@ -223,6 +224,11 @@ def nvfp4_get_device_status(stream=None):
 
 def nvfp4_status_string(status):
     return lib().nvfp4_status_string(status).decode()
+
+
+def nvfp4_debug_scale_recipe_check(counters, mismatch, stream=None):
+    _ok("nvfp4_debug_scale_recipe_check",
+        lib().nvfp4_debug_scale_recipe_check(_p(counters), _p(mismatch), _s(stream)))
 
 
 def nvfp4_debug_cvt_probe(first, last, counters, stream=None):

@@ -37,6 +37,42 @@ def test_init_data_classes(nv, orc, kind, M, K):
     assert_quant_equal(got, orc.quantize(x), what=f"{kind} {M}x{K}")
 
 
+@pytest.mark.parametrize("M,K", [(508, 256), (508, 768), (254, 2048), (64, 8192)])
+def test_rows_across_the_exponent_range(nv, orc, M, K):
+    """Row scales from bf16 subnormals up to the bf16 maximum, every biased
+    exponent at the top of some row, elements up to 40 binades below it: rows
+    whose outer scale lies outside [2^-90, 2^90] take the IEEE form of the
+    scale arithmetic, the others the FMA form; both give the oracle's bytes."""
+    rng = np.random.Generator(np.random.PCG64(M * 31 + K))
+    top = np.resize(np.arange(1, 255, dtype=np.int64), M) if M >= 254 else np.linspace(1, 254, M).astype(np.int64)
+    e = np.clip(top[:, None] - rng.integers(0, 41, size=(M, K)), 0, 254)
+    e[np.arange(M), rng.integers(0, K, size=M)] = top          # the row's top exponent is present
+    mant = rng.integers(0, 128, size=(M, K))
+    sign = rng.integers(0, 2, size=(M, K)) << 15
+    x = (sign | (e << 7) | mant).astype(np.uint16)
+    got = nv.quantize(to_dev(x))
+    assert_quant_equal(got, orc.quantize(x), what=f"exponent range {M}x{K}")
+
+
+def test_scale_recipe_fma_form_matches_ieee(nv):
+    """The FMA form of the block-scale quotient and reciprocal against the IEEE
+    intrinsics, on the GPU, over every (row amax, block amax <= row amax) pair of
+    bf16 values; the number of pairs compared is the count of rows in the FMA
+    range, computed here with numpy's IEEE binary32 division."""
+    cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
+    bad = torch.zeros(17, dtype=torch.int32, device="cuda")
+    nv.nvfp4_debug_scale_recipe_check(cnt, bad)
+    torch.cuda.synchronize()
+    c = cnt.cpu().numpy()
+    b = bad.cpu().numpy().view(np.uint32)
+    bits = np.arange(0x7F80, dtype=np.uint32)
+    S = (bits << np.uint32(16)).view(np.float32) / np.float32(2688.0)
+    fast = (S >= np.float32(2.0 ** -90)) & (S <= np.float32(2.0 ** 90))
+    assert int(c[0]) == int(np.sum(bits[fast].astype(np.int64) + 1))
+    pairs = [(hex(b[1 + 2 * k]), hex(b[2 + 2 * k])) for k in range(min(int(b[0]), 8))]
+    assert int(c[1]) == 0, f"{int(c[1])} pairs differ, first {pairs}"
+
+
 @pytest.mark.parametrize("M,K", [(96, 256), (160, 768), (400, 2048), (48, 4112)])
 def test_per_tensor_and_column_copy(nv, orc, M, K):
     x = W.small_matrix(M + 3 * K, M, K, dist="student_t3", outlier_cols=4, outlier_scale=50)
