@@ -76,6 +76,12 @@ constexpr uint32_t kATileBytes = kBM * kBKBytes;      // 16 KB
 constexpr uint32_t kSFAtomBytes = 512;                // 128 rows x 4 scales
 constexpr uint32_t kSFATileBytes = 4 * kSFAtomBytes;  // 2 KB per stage
 constexpr uint32_t kSFBTileBytes = 8 * kSFAtomBytes;  // 4 KB per stage
+// The swizzled scale arrays are read through 5D tensor maps
+// [experts][halves][128-row tiles][2 kgroups rows][256 bytes]: 8 rows of 256
+// bytes are the 4 atoms (2 KB) of one K step of one 128-row tile; a B box
+// takes two tiles (consecutive, or with SwiGLU the gate and the up tile).
+constexpr uint32_t kSFMapRowBytes = 256;
+constexpr uint32_t kSFMapBoxRows = kSFATileBytes / kSFMapRowBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSFTmemCol = 256;                  // after the 256 accumulator columns
 constexpr uint32_t kSFTmemPerStage = 48;              // 16 (A) + 32 (B)
@@ -146,10 +152,13 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+__device__ __forceinline__ void tma_load_5d(const CUtensorMap* map, uint64_t* bar, void* dst, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3, int32_t c4) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0),
+          "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
 }
 
@@ -509,7 +518,9 @@ template <bool kGrouped, bool kSwiGLU, bool kShortWaits>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                            const __grid_constant__ CUtensorMap tma_b,
-                           const __grid_constant__ CUtensorMap tma_y, GemmParams p) {
+                           const __grid_constant__ CUtensorMap tma_y,
+                           const __grid_constant__ CUtensorMap tma_sfa,
+                           const __grid_constant__ CUtensorMap tma_sfb, GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -544,7 +555,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int npairs = gridDim.x >> 1;
     const int num_pm = static_cast<int>((p.M + 255) / 256);
     const int a_row_tiles = static_cast<int>((p.M + 127) / 128);
-    const int sfb_tiles_n = static_cast<int>((p.N + 127) / 128);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPStages; ++s) {
@@ -623,11 +633,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             // Warp 0 loads A and its scales, warp kPBWarp this CTA's 128 rows of B
             // and the B scales; kPLoadLanes lanes of each split the rows.  (One
             // lane per warp with 128-row boxes measured as fast as two or four
-            // lanes with smaller boxes, and simpler.)
+            // lanes with smaller boxes, and simpler.)  The scale atoms come by
+            // tensor TMA too: with 2 KB non-tensor bulk copies the B producer,
+            // which issues two of them per K step, fell ~1,000 cycles behind the
+            // A producer and the K step took ~10% longer.
             const bool side_b = warp == kPBWarp;
             const int sub = lane;                     // which kPBoxRows-row part
             const CUtensorMap* map = side_b ? &tma_b : &tma_a;
+            const CUtensorMap* sf_map = side_b ? &tma_sfb : &tma_sfa;
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(sf_map)) : "memory");
             uint32_t stage = 0, phase = 0;
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
@@ -640,45 +655,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 const int64_t n0 = tl.n0;
                 const int a_tile = static_cast<int>(m0 / 128);
                 const bool a_sf_ok = a_tile < a_row_tiles;
-                // the B tile's two 128-row halves and their scale-atom columns:
-                // consecutive rows, or (SwiGLU) gate rows and the matching up rows
+                // the B tile's two 128-row halves: consecutive rows, or (SwiGLU)
+                // gate rows and the matching up rows; their scale atoms are one
+                // box of the B scale map at 128-row tile nt128 (of the expert)
                 const int nt128 = static_cast<int>(n0 / 128);
                 const int64_t b_half1 = kSwiGLU ? p.ffn : 128;
-                const int atom1 = nt128 + static_cast<int>(b_half1 / 128);
-                const bool two_b_atoms = kSwiGLU || atom1 < sfb_tiles_n;
-                const uint8_t* sfb_e = p.sfb + (kGrouped ? tl.expert * p.sfb_expert_bytes : 0);
+                const int32_t sf_expert = kGrouped ? static_cast<int32_t>(tl.expert) : 0;
                 for (int kt = 0; kt < p.num_k_tiles; ++kt) {
                     ok = __all_sync(kPLoadMask,
                                     wait_c(&empty[stage], phase ^ 1u));
                     if (!ok) break;
-                    const int ng = min(kMmaPerStage, p.kgroups - kt * kMmaPerStage);
-                    const uint32_t sf_bytes = ng * kSFAtomBytes;
                     const int64_t g0 = static_cast<int64_t>(kt) * kMmaPerStage;
-                    // lane 0 announces the side's bytes before any of its copies is issued
+                    // lane 0 announces the side's bytes before any of its copies is
+                    // issued (scale boxes are whole: past the last K group or the
+                    // last tile they hold the zero fill, unused)
                     if (sub == 0)
-                        mbar_arrive_expect_tx(&full[stage], side_b ? kPBHalfBytes + (two_b_atoms ? 2u : 1u) * sf_bytes
-                                                                   : kATileBytes + (a_sf_ok ? sf_bytes : 0u));
+                        mbar_arrive_expect_tx(&full[stage], side_b ? kPBHalfBytes + kSFBTileBytes
+                                                                   : kATileBytes + (a_sf_ok ? kSFATileBytes : 0u));
                     __syncwarp(kPLoadMask);
                     if (!side_b) {
                         tma_load_2d(map, &full[stage], sA + stage * kATileBytes + sub * kPBoxRows * kBKBytes,
                                     kt * kBKBytes, static_cast<int32_t>(m0 + kPBoxRows * sub));
                         if (a_sf_ok && sub == 0)
-                            bulk_load(sSFA + stage * kSFATileBytes,
-                                      p.sfa + (static_cast<int64_t>(a_tile) * p.kgroups + g0) * kSFAtomBytes,
-                                      sf_bytes, &full[stage]);
+                            tma_load_5d(sf_map, &full[stage], sSFA + stage * kSFATileBytes, 0,
+                                        static_cast<int32_t>(2 * g0), a_tile, 0, 0);
                     } else {
                         tma_load_2d(map, &full[stage], sB + stage * kPBHalfBytes + sub * kPBoxRows * kBKBytes,
                                     kt * kBKBytes,
                                     static_cast<int32_t>(tl.b_row0 + rank * b_half1 + kPBoxRows * sub));
-                        if (sub == 0) {
-                            bulk_load(sSFB + stage * kSFBTileBytes,
-                                      sfb_e + (static_cast<int64_t>(nt128) * p.kgroups + g0) * kSFAtomBytes, sf_bytes,
-                                      &full[stage]);
-                            if (two_b_atoms)
-                                bulk_load(sSFB + stage * kSFBTileBytes + kSFATileBytes,
-                                          sfb_e + (static_cast<int64_t>(atom1) * p.kgroups + g0) * kSFAtomBytes,
-                                          sf_bytes, &full[stage]);
-                        }
+                        if (sub == 0)
+                            tma_load_5d(sf_map, &full[stage], sSFB + stage * kSFBTileBytes, 0,
+                                        static_cast<int32_t>(2 * g0), nt128, 0, sf_expert);
                     }
                     issued_mask |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -1077,6 +1084,26 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_byte
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A swizzled scale array (kgroups K groups per 128-row tile, 512-byte atoms)
+// as [experts][halves][tiles][2 kgroups][256 bytes]; box = 8 rows (the four
+// atoms of one K step) of box_tiles x box_halves tiles, no swizzle.  Boxes that
+// reach past a dimension are zero-filled.
+bool make_map_sf(CUtensorMap* map, const void* base, int64_t kgroups, int64_t tiles, int64_t halves,
+                 int64_t experts, uint32_t box_tiles, uint32_t box_halves) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr || kgroups <= 0 || tiles <= 0 || halves <= 0 || experts <= 0) return false;
+    if (tiles > INT32_MAX || experts > INT32_MAX || 2 * kgroups > INT32_MAX) return false;
+    const cuuint64_t tile_bytes = static_cast<cuuint64_t>(kgroups) * kSFAtomBytes;
+    cuuint64_t dims[5] = {kSFMapRowBytes, static_cast<cuuint64_t>(2 * kgroups), static_cast<cuuint64_t>(tiles),
+                          static_cast<cuuint64_t>(halves), static_cast<cuuint64_t>(experts)};
+    cuuint64_t strides[4] = {kSFMapRowBytes, tile_bytes, tile_bytes * tiles, tile_bytes * tiles * halves};
+    cuuint32_t box[5] = {kSFMapRowBytes, kSFMapBoxRows, box_tiles, box_halves, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Y [rows x cols] bf16 with row pitch ld elements; box = 64 columns x 32 rows, 128-byte swizzle.
 bool make_map_y(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
     EncodeTiledFn fn = encode_fn();
@@ -1092,7 +1119,7 @@ bool make_map_y(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_
 
 template <bool kGrouped, bool kSwiGLU, bool kShortWaits>
 nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my,
-                              const GemmParams& p, int64_t pair_tiles, const DeviceCtx& ctx, cudaStream_t s) {
+                              const CUtensorMap& msfa, const CUtensorMap& msfb, const GemmParams& p, int64_t pair_tiles, const DeviceCtx& ctx, cudaStream_t s) {
     static unsigned long long attr_set[64] = {};   // per context: see ctx_cached
     if (!ctx_cached(attr_set, ctx)) {
         if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU, kShortWaits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1130,7 +1157,8 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU, kShortWaits>, ma, mb, my, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, nvfp4_gemm_pair_kernel<kGrouped, kSwiGLU, kShortWaits>, ma, mb, my, msfa, msfb, p) !=
+        cudaSuccess)
         return NVFP4_ERR_CUDA;
     return NVFP4_OK;
 }
@@ -1167,10 +1195,12 @@ nvfp4_status nvfp4_gemm_ex(const void* a_q, const void* a_sf, const float* a_s, 
     if (!aligned(a_q, 16) || !aligned(b_q, 16) || !aligned(a_sf, 16) || !aligned(b_sf, 16) ||
         !aligned(y, 16) || !aligned(a_s, 4) || !aligned(b_s, 4))
         return NVFP4_ERR_ALIGNMENT;
-    CUtensorMap ma, mb, my;
+    CUtensorMap ma, mb, my, msfa, msfb;
     // pairs of CTAs: each loads a 128-row half of the 256-row B tile
     if (!make_map(&ma, a_q, M, K / 2, kPBoxRows) || !make_map(&mb, b_q, N, K / 2, kPBoxRows) ||
-        !make_map_y(&my, y, M, N, ld_y))
+        !make_map_y(&my, y, M, N, ld_y) ||
+        !make_map_sf(&msfa, a_sf, K / 64, ceil_div(M, 128), 1, 1, 1, 1) ||
+        !make_map_sf(&msfb, b_sf, K / 64, ceil_div(N, 128), 1, 1, 2, 1))
         return NVFP4_ERR_CUDA;
     GemmParams p;
     p.sfa = static_cast<const uint8_t*>(a_sf);
@@ -1200,8 +1230,9 @@ nvfp4_status nvfp4_gemm_ex(const void* a_q, const void* a_sf, const float* a_s, 
     const int64_t pair_tiles = ceil_div(M, 256) * p.num_n_tiles;
     if (pair_tiles > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return p.wait_limit_ns == kWaitLimitNs ? launch_gemm_pair<false, false, false>(ma, mb, my, p, pair_tiles, ctx, s)
-                                           : launch_gemm_pair<false, false, true>(ma, mb, my, p, pair_tiles, ctx, s);
+    return p.wait_limit_ns == kWaitLimitNs
+               ? launch_gemm_pair<false, false, false>(ma, mb, my, msfa, msfb, p, pair_tiles, ctx, s)
+               : launch_gemm_pair<false, false, true>(ma, mb, my, msfa, msfb, p, pair_tiles, ctx, s);
 }
 
 nvfp4_status nvfp4_gemm(const void* a_q, const void* a_sf, const float* a_s, int64_t M,
@@ -1234,10 +1265,13 @@ nvfp4_status grouped_gemm(const void* a_q, const void* a_sf, const float* a_s, i
     if (!aligned(a_q, 16) || !aligned(b_q, 16) || !aligned(a_sf, 16) || !aligned(b_sf, 16) ||
         !aligned(y, 16) || !aligned(a_s, 4) || !aligned(b_s, 4) || !aligned(expert_offsets, 4))
         return NVFP4_ERR_ALIGNMENT;
-    CUtensorMap ma, mb, my;
+    CUtensorMap ma, mb, my, msfa, msfb;
     if (!make_map(&ma, a_q, rows_capacity, K / 2, kPBoxRows) ||
         !make_map(&mb, b_q, static_cast<int64_t>(E) * b_rows, K / 2, kPBoxRows) ||
-        !make_map_y(&my, y, rows_capacity, N, N))
+        !make_map_y(&my, y, rows_capacity, N, N) ||
+        !make_map_sf(&msfa, a_sf, K / 64, ceil_div(rows_capacity, 128), 1, 1, 1, 1) ||
+        !(swiglu ? make_map_sf(&msfb, b_sf, K / 64, N / 128, 2, E, 1, 2)
+                 : make_map_sf(&msfb, b_sf, K / 64, ceil_div(b_rows, 128), 1, E, 2, 1)))
         return NVFP4_ERR_CUDA;
     GemmParams p;
     p.sfa = static_cast<const uint8_t*>(a_sf);
@@ -1269,9 +1303,9 @@ nvfp4_status grouped_gemm(const void* a_q, const void* a_sf, const float* a_s, i
     if (slots > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
     const int64_t pair_tiles = (slots + 1) / 2;
     if (p.wait_limit_ns != kWaitLimitNs)   // debug: short pipeline waits (not for the SwiGLU epilogue)
-        return swiglu ? NVFP4_ERR_INVALID_ARG : launch_gemm_pair<true, false, true>(ma, mb, my, p, pair_tiles, ctx, stream);
-    return swiglu ? launch_gemm_pair<true, true, false>(ma, mb, my, p, pair_tiles, ctx, stream)
-                  : launch_gemm_pair<true, false, false>(ma, mb, my, p, pair_tiles, ctx, stream);
+        return swiglu ? NVFP4_ERR_INVALID_ARG : launch_gemm_pair<true, false, true>(ma, mb, my, msfa, msfb, p, pair_tiles, ctx, stream);
+    return swiglu ? launch_gemm_pair<true, true, false>(ma, mb, my, msfa, msfb, p, pair_tiles, ctx, stream)
+                  : launch_gemm_pair<true, false, false>(ma, mb, my, msfa, msfb, p, pair_tiles, ctx, stream);
 }
 
 }  // namespace
