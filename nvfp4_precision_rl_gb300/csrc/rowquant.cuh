@@ -113,11 +113,17 @@ struct Block16 {
     uint4 lo, hi;   // elements 0..7 and 8..15 of the block (bf16 pairs)
 };
 
+// max(|a|, |b|) per bf16 half, with the sign of a XOR b (max.xorsign.abs): the
+// magnitudes of a max tree need no masking until its root
+__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 __device__ __forceinline__ float block_absmax(const Block16& b) {
-    const uint32_t m = bmax2(bmax2(bmax2(b.lo.x & kAbsMask2, b.lo.y & kAbsMask2),
-                                   bmax2(b.lo.z & kAbsMask2, b.lo.w & kAbsMask2)),
-                             bmax2(bmax2(b.hi.x & kAbsMask2, b.hi.y & kAbsMask2),
-                                   bmax2(b.hi.z & kAbsMask2, b.hi.w & kAbsMask2)));
+    const uint32_t m = amax2(amax2(amax2(b.lo.x, b.lo.y), amax2(b.lo.z, b.lo.w)),
+                             amax2(amax2(b.hi.x, b.hi.y), amax2(b.hi.z, b.hi.w))) & kAbsMask2;
     return fmaxf(bf16lo(m), bf16hi(m));
 }
 
