@@ -370,26 +370,31 @@ __global__ void __launch_bounds__(512, 2) quant_row_pairs_kernel(RowJob job, Sta
         if (MODE == kAmaxOnly) continue;
         const ScaleRecipe rec0(MODE == kPerTensor ? tensor_amax : am0);
         const ScaleRecipe rec1(MODE == kPerTensor ? tensor_amax : am1);
-        uint2* q = reinterpret_cast<uint2*>(t.q);
+        // the pair's two code rows are consecutive: unit u is block u of the pair
+        uint2* const qpair = reinterpret_cast<uint2*>(t.q) + lr0 * nblocks;
+        // the pair's scale bytes: both rows lie in one 32-row group of a 128-row
+        // scale tile (lr0 even), row lr0 + 1 16 bytes after row lr0, group g of a
+        // row 512 g bytes after its group 0
+        uint8_t* const sfpair = t.sf + sf_word_offset(lr0, 0, kgroups);
         // the FMA form of the scale arithmetic when both rows allow it
         auto encode = [&](auto form) {
 #pragma unroll
             for (int i = 0; i < NU; ++i) {
                 const int u = i * 32 + lane;
                 const int h = hrow[i];
-                const int64_t lr = lr0 + h;
                 const int b = blk[i];
                 if (u >= 2 * nblocks) continue;
+                const uint32_t sfo = (static_cast<uint32_t>(h) << 4) + (static_cast<uint32_t>(b >> 2) << 9) + (b & 3);
                 if (h ? pad1 : pad0) {
                     // a pad row's scale words are zero (blocks 4g.. of its row, one byte each)
-                    if ((b >> 2) < kgroups) t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = 0;
+                    if ((b >> 2) < kgroups) sfpair[sfo] = 0;
                     continue;
                 }
                 float rb;
                 const uint32_t sb = (h ? rec1 : rec0).template block_as<decltype(form)::value>(bmax[i], &rb);
                 const float2 r2 = make_float2(rb, rb);
-                q[lr * nblocks + b] = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
-                t.sf[sf_word_offset(lr, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
+                qpair[u] = make_uint2(encode8(v[i].lo, r2), encode8(v[i].hi, r2));
+                sfpair[sfo] = static_cast<uint8_t>(sb);
             }
         };
         if (rec0.fast && rec1.fast) encode(std::true_type{});

@@ -146,6 +146,7 @@ __device__ __forceinline__ void encode_row_blocks(const Block16 (&v)[NB], const 
                                                   uint8_t* sf, float* s, int64_t r, int lane) {
     const ScaleRecipe rec(amax);
     uint2* qrow = q + r * nblocks;
+    uint8_t* const sfrow = sf + sf_word_offset(r, 0, kgroups);   // group g is 512 g bytes further
     auto encode = [&](auto form) {
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
@@ -157,7 +158,7 @@ __device__ __forceinline__ void encode_row_blocks(const Block16 (&v)[NB], const 
             if (b < nblocks) qrow[b] = w;
             // each lane writes its block's scale byte: four consecutive lanes
             // fill one swizzled word (blocks past the row's end write zero bytes)
-            if ((b >> 2) < kgroups) sf[sf_word_offset(r, b >> 2, kgroups) + (b & 3)] = static_cast<uint8_t>(sb);
+            if ((b >> 2) < kgroups) sfrow[(static_cast<uint32_t>(b >> 2) << 9) + (b & 3)] = static_cast<uint8_t>(sb);
         }
     };
     if (rec.fast) encode(std::true_type{});
