@@ -526,17 +526,20 @@ NVFP4_API nvfp4_status nvfp4_debug_cvt_probe(uint32_t* first, uint32_t* last, ui
                                    nvfp4_stream_t stream);
 
 /*
- * Self-check of the quantizers' scale arithmetic (block scale code and element
- * multiplier, "Towards Blackwell-Native 8-bit and 4-bit RL", "Bit-exact
- * quantizer contract"): rows whose outer scale lies in [2^-90, 2^90] compute the
- * correctly rounded quotient amax_b / T and reciprocal 1 / D with fused
- * multiply-adds instead of IEEE division.  This compares the two forms over
- * every pair of bf16 values the quantizers can meet (row amax, block amax <=
- * row amax; about 5e8 pairs).
+ * Self-check of the quantizers' scale arithmetic (outer scale, block scale code
+ * and element multiplier, "Towards Blackwell-Native 8-bit and 4-bit RL",
+ * "Bit-exact quantizer contract"): rows whose outer scale lies in [2^-90, 2^90]
+ * compute the correctly rounded quotients amax / 2688 and amax_b / T and the
+ * reciprocals 1 / T and 1 / D with fused multiply-adds instead of IEEE
+ * division.  This compares the two forms for every bf16 row amax and over every
+ * pair of bf16 values the quantizers can meet (row amax, block amax <= row
+ * amax; about 5e8 pairs).
  *  counters  uint64 [2] (device, 8-byte aligned): [0] pairs compared, [1]
- *            pairs whose code or multiplier differ (0 when the forms agree).
+ *            pairs whose code or multiplier differ, plus rows whose S, T, 1/T or
+ *            range decision differ (0 when the forms agree).
  *  mismatch  uint32 [17] (device): [0] mismatches recorded, then up to 8 pairs
- *            (row amax bits >> 16, block amax bits >> 16).
+ *            (row amax bits >> 16, block amax bits >> 16; 0xFFFFFFFF when the
+ *            row's own S, T, 1/T or range decision differ).
  * Both are cleared on the stream first; results are ready when it completes.
  */
 NVFP4_API nvfp4_status nvfp4_debug_scale_recipe_check(unsigned long long* counters, uint32_t* mismatch,

@@ -169,21 +169,35 @@ __global__ void __launch_bounds__(256) cvt_probe_kernel(uint32_t* first, uint32_
 }
 
 // Self-check of the scale recipe's two forms: block i takes the row amax with
-// bf16 bits i (every positive finite bf16 and zero: i = 0 .. 0x7F7F), its threads
-// every block amax a <= amax (bf16 bits j <= i); for a row in the FMA range the
-// FMA form's code and multiplier must equal the IEEE form's, bit for bit.
+// bf16 bits i (every positive finite bf16 and zero: i = 0 .. 0x7F7F); the row's
+// S, T, 1/T and FMA-range decision must equal the IEEE recipe's, and for a row
+// in the FMA range its threads take every block amax a <= amax (bf16 bits
+// j <= i), whose code and multiplier must equal the IEEE form's, bit for bit.
 // counters[0] = pairs compared (rows in the FMA range), counters[1] = mismatches;
 // mismatch[0] = how many were recorded, then up to 8 (i, j) pairs.
 __global__ void __launch_bounds__(256) recipe_check_kernel(unsigned long long* counters, uint32_t* mismatch) {
     const uint32_t i = blockIdx.x;
-    const ScaleRecipe rec(__uint_as_float(i << 16));
+    const float amax = __uint_as_float(i << 16);
+    const ScaleRecipe rec(amax);
+    const ScaleRecipe ref = ScaleRecipe::ieee(amax);
+    // the row's own quantities: the FMA range decision, S, T and 1/T
+    if (threadIdx.x == 0 && (rec.fast != ref.fast || __float_as_uint(rec.S) != __float_as_uint(ref.S) ||
+                             __float_as_uint(rec.T) != __float_as_uint(ref.T) ||
+                             __float_as_uint(rec.rcpT) != __float_as_uint(ref.rcpT))) {
+        atomicAdd(&counters[1], 1ull);
+        const uint32_t k = atomicAdd(mismatch, 1u);
+        if (k < 8) {
+            mismatch[1 + 2 * k] = i;
+            mismatch[2 + 2 * k] = 0xFFFFFFFFu;   // the row's recipe, not a block
+        }
+    }
     if (!rec.fast) return;
     unsigned long long n = 0, bad = 0;
     for (uint32_t j = threadIdx.x; j <= i; j += blockDim.x) {
         const float a = __uint_as_float(j << 16);
         float r_fma, r_ieee;
         const uint32_t s_fma = rec.block_as<true>(a, &r_fma);
-        const uint32_t s_ieee = rec.block_as<false>(a, &r_ieee);
+        const uint32_t s_ieee = ref.block_as<false>(a, &r_ieee);
         ++n;
         if (s_fma != s_ieee || __float_as_uint(r_fma) != __float_as_uint(r_ieee)) {
             ++bad;
