@@ -71,6 +71,9 @@ def parse_args():
                     help="run only the extra sections (small cases for profiling); prints their JSON")
     ap.add_argument("--moe-row-align", type=int, default=256, choices=[128, 256],
                     help="expert segment alignment of the MoE layout (256: one pair tile per slot)")
+    ap.add_argument("--moe-section-tokens", type=int, default=4096,
+                    help="tokens of the MoE section (c3): 4096, or more for a compute-bound case "
+                         "small enough to profile")
     return ap.parse_args()
 
 
@@ -725,7 +728,8 @@ def run_sections(args, torch, ops, W, dev, stream, tm, fp4_burst, hbm_gbs, check
                                                                hbm_gbs)
         launches += n
     if "c3" in secs:
-        out["qwen3_30b_a3b_moe_4096tok"], n = section_c3(torch, ops, W, dev, stream, tm, args, hbm_gbs)
+        out[f"qwen3_30b_a3b_moe_{args.moe_section_tokens}tok"], n = section_c3(torch, ops, W, dev, stream, tm, args,
+                                                                               hbm_gbs)
         launches += n
     check_status("after the sections")
     out["gpu_launches"] = launches
@@ -942,8 +946,9 @@ def section_c2(torch, ops, W, dev, stream, tm, args, fp4_burst, hbm_gbs):
 
 
 def section_c3(torch, ops, W, dev, stream, tm, args, hbm_gbs):
-    """The MoE expert step of the Qwen3-30B-A3B workload at 4096 tokens."""
-    wl = W.config3()
+    """The MoE expert step of the Qwen3-30B-A3B workload at 4096 tokens (or
+    --moe-section-tokens)."""
+    wl = W.config3(tokens=args.moe_section_tokens)
     moe = MoELayer(ops, torch, dev, stream, wl.moe, W.topk_weights(2, wl.moe.tokens, wl.moe.topk),
                    args.moe_row_align)
     st = moe.stages()
@@ -965,7 +970,7 @@ def section_c3(torch, ops, W, dev, stream, tm, args, hbm_gbs):
         if s.flop:
             r["tflops"] = round(s.flop / (seg[i] * 1e-3) / 1e12, 1)
         stages[s.name] = r
-    res = {"workload": "qwen3_30b_a3b_moe_4096tok_128e_top8 (hidden 2048, expert ffn 768)",
+    res = {"workload": f"qwen3_30b_a3b_moe_{wl.moe.tokens}tok_128e_top8 (hidden 2048, expert ffn 768)",
            "ms_per_step": round(tot, 5), "stage_graphs_ms": round(float(seg.sum()), 5),
            "tflops": round((fl1 + fl2) / (tot * 1e-3) / 1e12, 1),
            "routed_rows": moe.routed(), "layout_rows": moe.used_rows, "row_align": moe.align,
