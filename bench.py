@@ -468,7 +468,8 @@ class Timer:
 
 def one_way_bandwidth(torch, dev, flush):
     """Read-only and write-only DRAM bandwidth (GB/s) on this GPU, measured with
-    CUDA events: a sum over and a fill of 2 GB (best of five)."""
+    CUDA events: a sum over and a fill of 2 GB as 8-byte words (best of five;
+    a fill of bytes or 2-byte words is store-issue-bound at ~4 TB/s)."""
     buf = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
     words = buf.view(torch.int64)
 
@@ -486,7 +487,7 @@ def one_way_bandwidth(torch, dev, flush):
             ts.append(e0.elapsed_time(e1))
         return buf.numel() / (min(ts) * 1e-3) / 1e9
     rd = best(lambda: words.sum())
-    wr = best(lambda: buf.fill_(1))
+    wr = best(lambda: words.fill_(1))
     del buf, words
     torch.cuda.empty_cache()
     return rd, wr
@@ -688,7 +689,7 @@ def run_ours(args, rank, world, local_rank):
         "stages": stage_report,
         "one_graph_ms_per_step": round(float(t_one.mean()), 5),
         "hbm_one_way_gbs": {"read": round(rw_bw[0], 1), "write": round(rw_bw[1], 1),
-                            "how": "sum over / fill of 2 GB, best of five, CUDA events"},
+                            "how": "sum over / fill of 2 GB as int64 words, best of five, CUDA events"},
         "quantize": {"gbs": dense_percall["quantize_x_w"]["gbs"], "frac": dense_percall["quantize_x_w"]["frac"],
                      "hbm_peak_gbs": hbm_gbs, "peak_basis": f"{peak_src} copy bandwidth",
                      "what": "per-token X [65536, 2048] rows + W [6144, 2048] rows, one launch, per call",
