@@ -365,8 +365,8 @@ class MoELayer:
                 x, T, H, H, None, T, o.PER_TOKEN, self.xq["q"], self.xq["sf"], self.xq["s"], stream=s), 1,
                 nbytes=nb["quantize_tokens"], kernel="quant_rows_staged_kernel"),
             Stage("gather_quantized", lambda: o.nvfp4_moe_gather_quantized(
-                self.xq["q"], self.xq["sf"], self.xq["s"], T, H, self.gather, cap, self.a["q"], self.a["sf"],
-                self.a["s"], s), 1, nbytes=nb["gather_quantized"], kernel="gather_quantized_kernel"),
+                self.xq["q"], self.xq["sf"], self.xq["s"], T, H, self.gather, cap, self.off, E, self.a["q"],
+                self.a["sf"], self.a["s"], s), 1, nbytes=nb["gather_quantized"], kernel="gather_quantized_kernel"),
             # fc1 (gate + up) with SwiGLU in the GEMM epilogue: h [cap, F] bf16,
             # rows past the layout zero; then per-token quantization of h
             Stage("grouped_fc1_swiglu", lambda: o.nvfp4_grouped_gemm_swiglu(

@@ -265,13 +265,25 @@ NVFP4_API nvfp4_status nvfp4_moe_permute_noalloc(
  *  cols         > 0, % 16 == 0.
  *  gather_rows  int32 [rows_out] (device); an index >= rows_src makes a zero row
  *               and records NVFP4_ERR_DEVICE_INPUT.
+ *  expert_offsets  int32 [num_experts + 1] (device) or NULL: the layout's
+ *               expert offsets (nvfp4_moe_permute's output for these
+ *               gather_rows).  They set only the ORDER in which the 128-row
+ *               tiles are written, never the result: tile j of every expert,
+ *               then tile j + 1, so that the k copies of a token (whose rows sit
+ *               at about the same relative place in each expert, the permute
+ *               being stable in token order) are read while the token's row is
+ *               still in L2.  NULL, num_experts outside [1, 256] or offsets
+ *               that are negative or decreasing give the layout's own order.
+ *  num_experts  number of experts of expert_offsets (ignored when it is NULL).
  *  q, sf, s     uint8 [rows_out, cols/2], nvfp4_sf_bytes(rows_out, cols) bytes
  *               (scale rows past rows_out written as 0), float [rows_out].
- *  Pointers 16-byte aligned (s, s_src, gather_rows: 4).  rows_out == 0 is a no-op.
+ *  Pointers 16-byte aligned (s, s_src, gather_rows, expert_offsets: 4).
+ *  rows_out == 0 is a no-op.
  */
 NVFP4_API nvfp4_status nvfp4_moe_gather_quantized(
     const void* q_src, const void* sf_src, const float* s_src, int64_t rows_src, int64_t cols,
-    const int32_t* gather_rows, int64_t rows_out, void* q, void* sf, float* s, nvfp4_stream_t stream);
+    const int32_t* gather_rows, int64_t rows_out, const int32_t* expert_offsets, int32_t num_experts,
+    void* q, void* sf, float* s, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Block-scaled W4A4 GEMMs                                                   */

@@ -65,7 +65,7 @@ def lib():
         "nvfp4_quantize_per_token_pair": (st, [P, I64, I64, P, P, P, P, P, P, P, I64, I64, P, P, P, I64, P,
                                                SZ, P]),
         "nvfp4_moe_combine": (st, [P, I64, I64, P, P, I64, ctypes.c_int32, I64, P, I64, P]),
-        "nvfp4_moe_gather_quantized": (st, [P, P, P, I64, I64, P, I64, P, P, P, P]),
+        "nvfp4_moe_gather_quantized": (st, [P, P, P, I64, I64, P, I64, P, I32, P, P, P, P]),
         "nvfp4_mxfp8_sf_bytes": (SZ, [I64, I64]),
         "nvfp4_mxfp8_quantize": (st, [P, I64, I64, I64, P, P, P, P, P]),
         "nvfp4_mxfp8_dequantize": (st, [P, P, I64, I64, P, I64, P]),
@@ -192,11 +192,11 @@ def nvfp4_dequantize(q, sf, s, s_per_row, rows, cols, y, ld_y, stream=None):
         _p(q), _p(sf), _p(s), int(s_per_row), rows, cols, _p(y), ld_y, _s(stream)))
 
 
-def nvfp4_moe_gather_quantized(q_src, sf_src, s_src, rows_src, cols, gather_rows, rows_out, q, sf, s,
-                               stream=None):
+def nvfp4_moe_gather_quantized(q_src, sf_src, s_src, rows_src, cols, gather_rows, rows_out, expert_offsets,
+                               num_experts, q, sf, s, stream=None):
     _ok("nvfp4_moe_gather_quantized", lib().nvfp4_moe_gather_quantized(
-        _p(q_src), _p(sf_src), _p(s_src), rows_src, cols, _p(gather_rows), rows_out, _p(q), _p(sf), _p(s),
-        _s(stream)))
+        _p(q_src), _p(sf_src), _p(s_src), rows_src, cols, _p(gather_rows), rows_out, _p(expert_offsets),
+        num_experts, _p(q), _p(sf), _p(s), _s(stream)))
 
 
 def nvfp4_mxfp8_sf_bytes(rows, cols):
@@ -441,17 +441,19 @@ def dequantize(qres, column=False, out=None, stream=None):
     return y
 
 
-def moe_gather_quantized(qres, gather, stream=None):
+def moe_gather_quantized(qres, gather, offsets=None, stream=None):
     """Rows of a per-token quantize() result scattered to the routed layout
-    (row r = source row gather[r], zero row where gather[r] < 0)."""
+    (row r = source row gather[r], zero row where gather[r] < 0).  offsets, the
+    permute's expert offsets, only order the work (token-window order)."""
     rows_out = gather.shape[0]
     cols = qres["cols"]
     dev = qres["q"].device
     out = dict(rows=rows_out, cols=cols, q=_u8((rows_out, cols // 2), dev),
                sf=_u8(nvfp4_sf_bytes(rows_out, cols), dev),
                s=torch.empty(rows_out, dtype=torch.float32, device=dev))
-    nvfp4_moe_gather_quantized(qres["q"], qres["sf"], qres["s"], qres["rows"], cols, gather, rows_out, out["q"],
-                               out["sf"], out["s"], stream)
+    num_experts = 0 if offsets is None else offsets.numel() - 1
+    nvfp4_moe_gather_quantized(qres["q"], qres["sf"], qres["s"], qres["rows"], cols, gather, rows_out, offsets,
+                               num_experts, out["q"], out["sf"], out["s"], stream)
     return out
 
 

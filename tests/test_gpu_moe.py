@@ -60,11 +60,46 @@ def test_gather_quantized_bit_exact(nv, orc, T, H, E, k, align):
     ids = _ids(24 + T, T, E, k)
     perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E, row_align=align)
     rperm = orc.moe_permute(ids, E, align, capacity=perm["capacity"])
-    got = nv.moe_gather_quantized(nv.quantize(to_dev(x)), perm["gather"])
+    got = nv.moe_gather_quantized(nv.quantize(to_dev(x)), perm["gather"], perm["offsets"])
     torch.cuda.synchronize()
     assert nv.nvfp4_get_device_status() == 0
     ref = orc.quantize(x, gather=rperm["gather"])
     assert_quant_equal(got, ref, what="gather of quantized rows")
+
+
+@pytest.mark.parametrize("T,H,E,k,align", [(300, 512, 16, 4, 128), (4096, 2048, 128, 8, 256)])
+@pytest.mark.parametrize("order", ["none", "foreign", "unaligned", "decreasing", "too_many"])
+def test_gather_quantized_tile_order(nv, orc, T, H, E, k, align, order):
+    """The expert offsets only order the tiles: with none, with offsets of
+    another layout (non-decreasing, starting past 0, ending short of the rows),
+    with unaligned or decreasing ones, or more experts than the order handles,
+    every byte is the same as the oracle's gather-quantize."""
+    x = W.small_matrix(25 + T, T, H, dist="lognormal_rows")
+    ids = _ids(26 + T, T, E, k)
+    perm = nv.moe_permute(torch.from_numpy(ids).cuda(), E, row_align=align)
+    rows = perm["capacity"]
+    rng = np.random.default_rng(27 + T)
+    if order == "none":
+        offs = None
+    elif order == "foreign":
+        o = np.sort(rng.integers(128, max(rows - 200, 129), size=E + 1)).astype(np.int32)
+        offs = torch.from_numpy(o).cuda()
+    elif order == "unaligned":
+        o = np.sort(rng.integers(0, rows + 1000, size=E + 1)).astype(np.int32)
+        o[0] = 3
+        offs = torch.from_numpy(o).cuda()
+    elif order == "decreasing":
+        o = host(perm["offsets"]).copy()
+        o[E // 2] = o[E // 2 + 1] + 1
+        offs = torch.from_numpy(o).cuda()
+    else:
+        offs = torch.arange(0, 300 * 128, 128, dtype=torch.int32, device="cuda")   # 299 experts
+    got = nv.moe_gather_quantized(nv.quantize(to_dev(x)), perm["gather"], offs)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_status() == 0
+    rperm = orc.moe_permute(ids, E, align, capacity=rows)
+    ref = orc.quantize(x, gather=rperm["gather"])
+    assert_quant_equal(got, ref, what=f"gather of quantized rows ({order} order)")
 
 
 def test_gather_quantized_bad_index(nv):

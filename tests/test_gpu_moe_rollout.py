@@ -38,7 +38,7 @@ def rollout(nv, orc):
     ids = torch.from_numpy(m.topk_ids).cuda()
     perm = nv.moe_permute(ids, m.experts, row_align=ALIGN)
     xq = nv.quantize(to_dev(m.x))
-    a = nv.moe_gather_quantized(xq, perm["gather"])
+    a = nv.moe_gather_quantized(xq, perm["gather"], perm["offsets"])
     torch.cuda.synchronize()
     assert nv.nvfp4_get_device_status() == 0
     rperm = orc.moe_permute(m.topk_ids, m.experts, ALIGN, capacity=perm["capacity"])
@@ -145,7 +145,7 @@ def test_grouped_fc2_rollout_every_expert(nv, orc, rollout):
     layout by the same permutation)."""
     m = rollout["m"]
     h = W.random_bf16_bits(52, (m.tokens, m.ffn), exp_lo=118, exp_hi=128)
-    hq = nv.moe_gather_quantized(nv.quantize(to_dev(h)), rollout["perm"]["gather"])
+    hq = nv.moe_gather_quantized(nv.quantize(to_dev(h)), rollout["perm"]["gather"], rollout["perm"]["offsets"])
     _grouped_every_expert(nv, orc, hq, orc.quantize(h), rollout["perm"], rollout["rperm"], m.w2,
                           m.hidden, m.ffn, seed=53)
 
