@@ -188,7 +188,7 @@ NVFP4_API nvfp4_status nvfp4_quantize_per_token_pair(
  * (row_align - 1), rounded up to row_align. */
 NVFP4_API int64_t nvfp4_moe_capacity(int64_t tokens, int32_t topk, int32_t num_experts, int32_t row_align);
 
-/* Scratch bytes of nvfp4_moe_permute (per-chunk expert histograms). */
+/* Scratch bytes of nvfp4_moe_permute (per-expert totals and per-chunk expert histograms). */
 NVFP4_API size_t nvfp4_moe_permute_workspace_bytes(int64_t tokens, int32_t topk, int32_t num_experts);
 
 /*
@@ -233,7 +233,7 @@ NVFP4_API nvfp4_status nvfp4_moe_permute(
  * process exits.
  *
  *  Limit: nvfp4_moe_permute_workspace_bytes(tokens, topk, num_experts) must be
- *  <= 1 MiB (for 128 experts: up to 2,097,152 routed (token, slot) pairs);
+ *  <= 1 MiB (for 128 experts: up to 2,096,128 routed (token, slot) pairs);
  *  larger sizes return NVFP4_ERR_WORKSPACE and launch nothing.
  *  The first call on a device (and the first in each further CUDA context on
  *  it) looks up the array's device address, with that device current, and so

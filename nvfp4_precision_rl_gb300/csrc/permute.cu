@@ -4,10 +4,11 @@
 // order, with all metadata left on the device ("miniTE report", section
 // "Transformer Engine path optimisation": contiguous layouts and device-side
 // metadata feed the grouped GEMM without a host round trip).
-//   1. count:   one block per chunk of kChunk pairs -> per-chunk expert histogram
-//   2. scan:    one block of 1024 threads (experts x groups of chunks):
-//               per-expert totals, padded exclusive scan -> offsets, and each
-//               chunk's first row inside each expert segment
+//   1. count:   one block per chunk of kChunk pairs -> per-chunk expert histogram,
+//               and the per-expert totals (atomic adds of the block histograms)
+//   2. scan:    one block per expert: the padded sizes of the experts before it
+//               -> its segment start (offsets), then an exclusive scan of its
+//               column of chunk counts -> each chunk's first row in the segment
 //   3. scatter: one block per chunk, in order: rank inside the chunk from
 //               warp match + per-warp histograms -> gather_rows / dst_rows
 #include <mutex>
@@ -22,7 +23,7 @@ constexpr int kPermThreads = 256;
 constexpr int kMaxExperts = 1024;
 
 __global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t* ids, int64_t n,
-                                                                  int E, int32_t* counts,
+                                                                  int E, int32_t* counts, int32_t* totals,
                                                                   unsigned* status) {
     extern __shared__ int32_t s_hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
@@ -35,96 +36,68 @@ __global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t*
         else record_error(status, NVFP4_ERR_DEVICE_INPUT, DETAIL_EXPERT_ID);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        counts[static_cast<int64_t>(blockIdx.x) * E + e] = s_hist[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t h = s_hist[e];
+        counts[static_cast<int64_t>(blockIdx.x) * E + e] = h;
+        if (h != 0) atomicAdd(totals + e, h);
+    }
 }
 
-// One block of kScanThreads threads: Ew = round_up(E, 32) experts across and
-// G = kScanThreads / Ew groups of chunks down; thread (g, e) sums expert e's
-// counts over its group's chunks (loads batched so that many are in flight),
-// the first Ew threads scan the padded totals, then every thread rewrites its
-// chunks' counts as their first rows in the expert segment.
-constexpr int kScanThreads = 1024;
-constexpr int kScanBatch = 8;
-
-__global__ void __launch_bounds__(kScanThreads) perm_scan_kernel(int32_t* counts, int nchunks, int E, int align,
-                                                                 int32_t* offsets) {
-    __shared__ int32_t s_part[kScanThreads];   // [G][Ew] per-group sums, then per-group bases
-    __shared__ int32_t s_warp[32];
-    const int Ew = (E + 31) & ~31;
-    const int G = kScanThreads / Ew;
-    const int e = threadIdx.x % Ew;
-    const int g = threadIdx.x / Ew;
-    const bool mine = g < G && e < E;
-    const int per = (nchunks + G - 1) / G;
-    const int c0 = g * per;
-    const int c1 = min(c0 + per, nchunks);
-    int32_t sum = 0;
-    if (mine) {
-        for (int c = c0; c < c1; c += kScanBatch) {
-            int32_t v[kScanBatch];
+// Exclusive scan of one value per thread over the block (blockDim.x a multiple
+// of 32, at most 1024); returns the thread's exclusive prefix and the block sum.
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* total, int64_t* s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int64_t incl = v;
 #pragma unroll
-            for (int j = 0; j < kScanBatch; ++j)
-                v[j] = (c + j < c1) ? counts[static_cast<int64_t>(c + j) * E + e] : 0;
-#pragma unroll
-            for (int j = 0; j < kScanBatch; ++j) sum += v[j];
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
     }
-    if (g < G) s_part[g * Ew + e] = sum;
-    __syncthreads();
-    // the first Ew threads (whole warps): expert totals, padded, block-wide exclusive scan
-    int32_t padded = 0, incl = 0;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x < Ew) {
-        int64_t total = 0;
-        for (int gg = 0; gg < G; ++gg) total += s_part[gg * Ew + e];
-        padded = (e < E) ? static_cast<int32_t>((total + align - 1) / align * align) : 0;
-        incl = padded;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        if (lane == 31) s_warp[warp] = incl;
-    }
+    if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const int nw = Ew >> 5;
-        int32_t w = lane < nw ? s_warp[lane] : 0;
+        int64_t w = lane < nw ? s_warp[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int32_t t = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            const int64_t t = __shfl_up_sync(0xFFFFFFFFu, w, o);
             if (lane >= o) w += t;
         }
         if (lane < nw) s_warp[lane] = w;   // inclusive over warps
     }
     __syncthreads();
-    if (threadIdx.x < Ew && e < E) {
-        const int32_t excl = incl - padded + (warp > 0 ? s_warp[warp - 1] : 0);
-        offsets[e] = excl;
-        if (e == E - 1) offsets[E] = excl + padded;
-        // group gg of expert e starts after the segment start and the earlier groups
-        int32_t base = excl;
-        for (int gg = 0; gg < G; ++gg) {
-            const int32_t part = s_part[gg * Ew + e];
-            s_part[gg * Ew + e] = base;
-            base += part;
-        }
+    const int64_t excl = incl - v + (warp > 0 ? s_warp[warp - 1] : 0);
+    *total = s_warp[nw - 1];
+    __syncthreads();   // s_warp is reused by the next call
+    return excl;
+}
+
+// One block per expert e: its segment starts after the padded sizes of experts
+// 0 .. e-1 (from the count pass's totals); chunk c's first row in the segment
+// is the start plus the counts of expert e in chunks 0 .. c-1, written over
+// counts[c][e] (only this block reads or writes column e).
+constexpr int kScanThreads = 512;
+
+__global__ void __launch_bounds__(kScanThreads) perm_scan_kernel(int32_t* counts, const int32_t* totals, int nchunks,
+                                                                 int E, int align, int32_t* offsets) {
+    __shared__ int64_t s_warp[kScanThreads / 32];
+    const int e = blockIdx.x;
+    auto padded = [align](int32_t t) { return (static_cast<int64_t>(t) + align - 1) / align * align; };
+    int64_t part = 0;
+    for (int j = threadIdx.x; j < e; j += blockDim.x) part += padded(totals[j]);
+    int64_t start = 0;
+    (void)block_exclusive_scan(part, &start, s_warp);
+    if (threadIdx.x == 0) {
+        offsets[e] = static_cast<int32_t>(start);
+        if (e == E - 1) offsets[E] = static_cast<int32_t>(start + padded(totals[e]));
     }
-    __syncthreads();
-    if (mine) {
-        int32_t base = s_part[g * Ew + e];
-        for (int c = c0; c < c1; c += kScanBatch) {
-            int32_t v[kScanBatch];
-#pragma unroll
-            for (int j = 0; j < kScanBatch; ++j)
-                v[j] = (c + j < c1) ? counts[static_cast<int64_t>(c + j) * E + e] : 0;
-#pragma unroll
-            for (int j = 0; j < kScanBatch; ++j) {
-                if (c + j < c1) counts[static_cast<int64_t>(c + j) * E + e] = base;
-                base += v[j];
-            }
-        }
+    int64_t carry = start;
+    for (int c0 = 0; c0 < nchunks; c0 += blockDim.x) {
+        const int c = c0 + threadIdx.x;
+        const int64_t v = c < nchunks ? counts[static_cast<int64_t>(c) * E + e] : 0;
+        int64_t sum = 0;
+        const int64_t excl = block_exclusive_scan(v, &sum, s_warp);
+        if (c < nchunks) counts[static_cast<int64_t>(c) * E + e] = static_cast<int32_t>(carry + excl);
+        carry += sum;
     }
 }
 
@@ -188,8 +161,8 @@ int64_t nvfp4_moe_capacity(int64_t tokens, int32_t topk, int32_t num_experts, in
 size_t nvfp4_moe_permute_workspace_bytes(int64_t tokens, int32_t topk, int32_t num_experts) {
     if (tokens < 0 || topk <= 0 || num_experts <= 0) return 0;
     const int64_t chunks = ceil_div(tokens * topk, kChunk);
-    const int64_t bytes = chunks * num_experts * 4;
-    return static_cast<size_t>(bytes < 256 ? 256 : bytes);
+    // per-expert totals (padded to 256 bytes), then the per-chunk histograms
+    return static_cast<size_t>(round_up(static_cast<int64_t>(num_experts), 64) * 4 + chunks * num_experts * 4);
 }
 
 nvfp4_status nvfp4_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t topk,
@@ -216,17 +189,19 @@ nvfp4_status nvfp4_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t 
         return NVFP4_ERR_WORKSPACE;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int32_t* counts = static_cast<int32_t*>(workspace);
     const int nchunks = static_cast<int>(ceil_div(n, kChunk));
     const int E = num_experts;
-    if (cudaMemsetAsync(gather_rows, 0xFF, static_cast<size_t>(capacity) * 4, s) != cudaSuccess)
+    int32_t* totals = static_cast<int32_t*>(workspace);
+    int32_t* counts = totals + round_up(static_cast<int64_t>(E), 64);
+    if (cudaMemsetAsync(gather_rows, 0xFF, static_cast<size_t>(capacity) * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(totals, 0, static_cast<size_t>(E) * 4, s) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     if (nchunks > 0) {
-        perm_count_kernel<<<nchunks, kPermThreads, E * sizeof(int32_t), s>>>(topk_ids, n, E, counts,
+        perm_count_kernel<<<nchunks, kPermThreads, E * sizeof(int32_t), s>>>(topk_ids, n, E, counts, totals,
                                                                                ctx.status);
         NVFP4_CHECK_LAUNCH();
     }
-    perm_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, nchunks, E, row_align, expert_offsets);
+    perm_scan_kernel<<<E, kScanThreads, 0, s>>>(counts, totals, nchunks, E, row_align, expert_offsets);
     NVFP4_CHECK_LAUNCH();
     if (nchunks > 0) {
         const size_t smem = static_cast<size_t>(E) * (1 + kPermThreads / 32) * sizeof(int32_t);
