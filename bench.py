@@ -375,7 +375,7 @@ class MoELayer:
                 kernel="nvfp4_gemm_pair_kernel<1, 1, 0>"),
             Stage("quantize_h", lambda: o.nvfp4_quantize_per_token(
                 self.h, cap, F, F, None, cap, o.PER_TOKEN, self.hq["q"], self.hq["sf"], self.hq["s"], stream=s), 1,
-                nbytes=nb["quantize_h"], kernel="quant_rows_staged_kernel (768 columns)"),
+                nbytes=nb["quantize_h"], kernel="quant_row_pairs_kernel (768 columns)"),
             Stage("grouped_fc2", lambda: o.nvfp4_grouped_gemm(
                 self.hq["q"], self.hq["sf"], self.hq["s"], cap, self.off, E, self.w2["q"], self.w2["sf"],
                 self.w2["s"], H, F, self.y2, s), 1, flop=fl2, nbytes=nb["grouped_fc2"],

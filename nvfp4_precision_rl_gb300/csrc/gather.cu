@@ -97,13 +97,13 @@ __device__ void build_tile_order(TileOrder* o, const int32_t* __restrict__ offse
     __syncthreads();
 }
 
-// One CTA per 128-row tile of the output (a tile of the swizzled scale layout,
-// visited in TileOrder):
-// the tile's source rows are read once into shared memory; the codes are
-// copied in 16- (or 8-) byte pieces, the lanes of a warp on consecutive pieces
-// of a row, four rows' loads in flight before their stores; each 512-byte
-// scale atom (128 rows x one word) is written as 32 16-byte lines, lane l
-// gathering the words of rows l, l+32, l+64, l+96.
+// One CTA per 128-row tile of the output (a tile of the swizzled scale layout),
+// tiles visited in TileOrder: the tile's 128 source row indices are read once
+// into shared memory; the codes are copied in 16- (or 8-) byte pieces, the
+// lanes of a warp on consecutive pieces of a row, four rows' loads in flight
+// before their stores; each 512-byte scale atom (128 rows x one word) is
+// written as 32 16-byte lines, lane l gathering the words of rows l, l+32,
+// l+64, l+96.
 template <bool kVec16>
 __global__ void __launch_bounds__(kGqThreads) gather_quantized_kernel(
     const uint8_t* __restrict__ q_src, const uint8_t* __restrict__ sf_src, const float* __restrict__ s_src,
