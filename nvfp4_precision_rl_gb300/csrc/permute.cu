@@ -9,6 +9,7 @@
 //   2. scan:    one block per expert: the padded sizes of the experts before it
 //               -> its segment start (offsets), then an exclusive scan of its
 //               column of chunk counts -> each chunk's first row in the segment
+//               (up to 64 chunks: one block over the whole histogram instead)
 //   3. scatter: one block per chunk, in order: rank inside the chunk from
 //               warp match + per-warp histograms -> gather_rows / dst_rows
 #include <mutex>
@@ -39,7 +40,98 @@ __global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t*
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int32_t h = s_hist[e];
         counts[static_cast<int64_t>(blockIdx.x) * E + e] = h;
-        if (h != 0) atomicAdd(totals + e, h);
+        if (totals != nullptr && h != 0) atomicAdd(totals + e, h);
+    }
+}
+
+// Small histograms (up to kScanOneMaxChunks chunks): one block of
+// kScanOneThreads threads: Ew = round_up(E, 32) experts across and
+// G = kScanOneThreads / Ew groups of chunks down; thread (g, e) sums expert e's
+// counts over its group's chunks (loads batched so that many are in flight),
+// the first Ew threads scan the padded totals, then every thread rewrites its
+// chunks' counts as their first rows in the expert segment.
+constexpr int kScanOneThreads = 1024;
+constexpr int kScanOneMaxChunks = 64;
+constexpr int kScanBatch = 8;
+
+__global__ void __launch_bounds__(kScanOneThreads) perm_scan_one_block_kernel(int32_t* counts, int nchunks, int E, int align,
+                                                                 int32_t* offsets) {
+    __shared__ int32_t s_part[kScanOneThreads];   // [G][Ew] per-group sums, then per-group bases
+    __shared__ int32_t s_warp[32];
+    const int Ew = (E + 31) & ~31;
+    const int G = kScanOneThreads / Ew;
+    const int e = threadIdx.x % Ew;
+    const int g = threadIdx.x / Ew;
+    const bool mine = g < G && e < E;
+    const int per = (nchunks + G - 1) / G;
+    const int c0 = g * per;
+    const int c1 = min(c0 + per, nchunks);
+    int32_t sum = 0;
+    if (mine) {
+        for (int c = c0; c < c1; c += kScanBatch) {
+            int32_t v[kScanBatch];
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j)
+                v[j] = (c + j < c1) ? counts[static_cast<int64_t>(c + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) sum += v[j];
+        }
+    }
+    if (g < G) s_part[g * Ew + e] = sum;
+    __syncthreads();
+    // the first Ew threads (whole warps): expert totals, padded, block-wide exclusive scan
+    int32_t padded = 0, incl = 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x < Ew) {
+        int64_t total = 0;
+        for (int gg = 0; gg < G; ++gg) total += s_part[gg * Ew + e];
+        padded = (e < E) ? static_cast<int32_t>((total + align - 1) / align * align) : 0;
+        incl = padded;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = Ew >> 5;
+        int32_t w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += t;
+        }
+        if (lane < nw) s_warp[lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    if (threadIdx.x < Ew && e < E) {
+        const int32_t excl = incl - padded + (warp > 0 ? s_warp[warp - 1] : 0);
+        offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + padded;
+        // group gg of expert e starts after the segment start and the earlier groups
+        int32_t base = excl;
+        for (int gg = 0; gg < G; ++gg) {
+            const int32_t part = s_part[gg * Ew + e];
+            s_part[gg * Ew + e] = base;
+            base += part;
+        }
+    }
+    __syncthreads();
+    if (mine) {
+        int32_t base = s_part[g * Ew + e];
+        for (int c = c0; c < c1; c += kScanBatch) {
+            int32_t v[kScanBatch];
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j)
+                v[j] = (c + j < c1) ? counts[static_cast<int64_t>(c + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) {
+                if (c + j < c1) counts[static_cast<int64_t>(c + j) * E + e] = base;
+                base += v[j];
+            }
+        }
     }
 }
 
@@ -71,7 +163,7 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* tota
     return excl;
 }
 
-// One block per expert e: its segment starts after the padded sizes of experts
+// Larger histograms: one block per expert e.  Its segment starts after the padded sizes of experts
 // 0 .. e-1 (from the count pass's totals); chunk c's first row in the segment
 // is the start plus the counts of expert e in chunks 0 .. c-1, written over
 // counts[c][e] (only this block reads or writes column e).
@@ -193,15 +285,22 @@ nvfp4_status nvfp4_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t 
     const int E = num_experts;
     int32_t* totals = static_cast<int32_t*>(workspace);
     int32_t* counts = totals + round_up(static_cast<int64_t>(E), 64);
+    // a few chunks: one scan block reads the whole histogram (no totals);
+    // more: the count pass also sums per-expert totals and one block per
+    // expert scans its column
+    const bool one_block = nchunks <= kScanOneMaxChunks;
     if (cudaMemsetAsync(gather_rows, 0xFF, static_cast<size_t>(capacity) * 4, s) != cudaSuccess ||
-        cudaMemsetAsync(totals, 0, static_cast<size_t>(E) * 4, s) != cudaSuccess)
+        (!one_block && cudaMemsetAsync(totals, 0, static_cast<size_t>(E) * 4, s) != cudaSuccess))
         return NVFP4_ERR_CUDA;
     if (nchunks > 0) {
-        perm_count_kernel<<<nchunks, kPermThreads, E * sizeof(int32_t), s>>>(topk_ids, n, E, counts, totals,
-                                                                               ctx.status);
+        perm_count_kernel<<<nchunks, kPermThreads, E * sizeof(int32_t), s>>>(
+            topk_ids, n, E, counts, one_block ? nullptr : totals, ctx.status);
         NVFP4_CHECK_LAUNCH();
     }
-    perm_scan_kernel<<<E, kScanThreads, 0, s>>>(counts, totals, nchunks, E, row_align, expert_offsets);
+    if (one_block)
+        perm_scan_one_block_kernel<<<1, kScanOneThreads, 0, s>>>(counts, nchunks, E, row_align, expert_offsets);
+    else
+        perm_scan_kernel<<<E, kScanThreads, 0, s>>>(counts, totals, nchunks, E, row_align, expert_offsets);
     NVFP4_CHECK_LAUNCH();
     if (nchunks > 0) {
         const size_t smem = static_cast<size_t>(E) * (1 + kPermThreads / 32) * sizeof(int32_t);
