@@ -57,7 +57,8 @@ __device__ __forceinline__ int64_t tile_of(const TileOrder& o, int64_t k) {
 // Fills *o from the expert offsets (all threads of the CTA call it; E = 0 when
 // there are none or they are unusable: the identity order).
 __device__ void build_tile_order(TileOrder* o, const int32_t* __restrict__ offsets, int num_experts, int64_t tiles) {
-    const int E = (offsets != nullptr && num_experts >= 1 && num_experts <= kGqMaxExperts) ? num_experts : 0;
+    const int E = (offsets != nullptr && num_experts >= 1 && num_experts <= kGqMaxExperts && tiles <= 0x7FFFFFFF)
+                      ? num_experts : 0;
     bool good = true;
     for (int e = threadIdx.x; e <= E && E > 0; e += blockDim.x) {
         const int32_t off = __ldg(offsets + e);
