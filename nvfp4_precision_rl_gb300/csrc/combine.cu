@@ -7,7 +7,9 @@
 // The reduction is binary32 in slot order, multiply then add, each one IEEE
 // operation (__fmul_rn / __fadd_rn: never contracted into an FMA), so the
 // result is bit-exact.  Memory-bound gather: one thread per (token, 8 columns),
-// the topk 16-byte rows loads issued before any arithmetic.
+// the topk 16-byte row loads issued before any arithmetic; with topk fixed at
+// compile time, the next item's rows and weights are read while the current
+// item's rows load, so each item waits on one memory latency instead of two.
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -25,6 +27,61 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(const uint16_t* __r
     const int topk = kTopk > 0 ? kTopk : topk_rt;
     const int64_t total = tokens * chunks;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if constexpr (kTopk > 0) {
+        // the rows and weights of the next item are read while the current one's rows load
+        int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        int32_t rn[kTopk];
+        float wn[kTopk];
+        auto fetch = [&](int64_t it) {
+            const int64_t t = it / chunks;
+#pragma unroll
+            for (int u = 0; u < kTopk; ++u) {
+                rn[u] = it < total ? __ldg(dst + t * kTopk + u) : -1;
+                wn[u] = it < total ? __ldg(w + t * kTopk + u) : 0.0f;
+            }
+        };
+        fetch(i);
+        for (; i < total; i += stride) {
+            const int64_t t = i / chunks;
+            const int c = static_cast<int>(i - t * chunks);
+            int32_t r[kTopk];
+            float wj[kTopk];
+#pragma unroll
+            for (int u = 0; u < kTopk; ++u) {
+                r[u] = rn[u];
+                wj[u] = wn[u];
+            }
+            uint4 v[kTopk];
+#pragma unroll
+            for (int u = 0; u < kTopk; ++u) {
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (r[u] >= 0 && r[u] < rows) v[u] = __ldg(reinterpret_cast<const uint4*>(y2 + r[u] * ld_y2) + c);
+                else if (c == 0) record_error(status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
+            }
+            fetch(i + stride);
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+            for (int u = 0; u < kTopk; ++u) {
+                if (r[u] < 0 || r[u] >= rows) continue;   // contributes nothing
+                const uint32_t words[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj[u], bf16lo(words[e])));
+                    acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj[u], bf16hi(words[e])));
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+                o[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            reinterpret_cast<uint4*>(out + t * ld_out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        return;
+    }
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
         const int64_t t = i / chunks;
         const int c = static_cast<int>(i - t * chunks);
