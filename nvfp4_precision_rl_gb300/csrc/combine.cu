@@ -6,10 +6,12 @@
 // routed experts' outputs pass through a high-precision weighted reduction.)
 // The reduction is binary32 in slot order, multiply then add, each one IEEE
 // operation (__fmul_rn / __fadd_rn: never contracted into an FMA), so the
-// result is bit-exact.  Memory-bound gather: one thread per (token, 8 columns),
-// the topk 16-byte row loads issued before any arithmetic; with topk fixed at
-// compile time, the next item's rows and weights are read while the current
-// item's rows load, so each item waits on one memory latency instead of two.
+// result is bit-exact.  Memory-bound gather: one thread per (token, 8 columns)
+// -- with topk fixed at compile time (and an even number of 8-column chunks),
+// per (token, chunks c and c + chunks / 2) -- the topk 16-byte row loads
+// issued before any arithmetic; in the fixed-topk kernel the next item's rows
+// and weights are read while the current item's rows load, so each item waits
+// on one memory latency instead of two.
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -28,22 +30,25 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(const uint16_t* __r
     const int64_t total = tokens * chunks;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if constexpr (kTopk > 0) {
-        // the rows and weights of the next item are read while the current one's rows load
+        // two chunks per item (c and c + chunks / 2 of one token): the next
+        // item's rows and weights are read while the current one's rows load
+        const int half = chunks >> 1;
+        const int64_t items = tokens * half;
         int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
         int32_t rn[kTopk];
         float wn[kTopk];
         auto fetch = [&](int64_t it) {
-            const int64_t t = it / chunks;
+            const int64_t t = it / half;
 #pragma unroll
             for (int u = 0; u < kTopk; ++u) {
-                rn[u] = it < total ? __ldg(dst + t * kTopk + u) : -1;
-                wn[u] = it < total ? __ldg(w + t * kTopk + u) : 0.0f;
+                rn[u] = it < items ? __ldg(dst + t * kTopk + u) : -1;
+                wn[u] = it < items ? __ldg(w + t * kTopk + u) : 0.0f;
             }
         };
         fetch(i);
-        for (; i < total; i += stride) {
-            const int64_t t = i / chunks;
-            const int c = static_cast<int>(i - t * chunks);
+        for (; i < items; i += stride) {
+            const int64_t t = i / half;
+            const int c = static_cast<int>(i - t * half);
             int32_t r[kTopk];
             float wj[kTopk];
 #pragma unroll
@@ -51,34 +56,43 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(const uint16_t* __r
                 r[u] = rn[u];
                 wj[u] = wn[u];
             }
-            uint4 v[kTopk];
+            uint4 v[kTopk][2];
 #pragma unroll
             for (int u = 0; u < kTopk; ++u) {
-                v[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (r[u] >= 0 && r[u] < rows) v[u] = __ldg(reinterpret_cast<const uint4*>(y2 + r[u] * ld_y2) + c);
-                else if (c == 0) record_error(status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
-            }
-            fetch(i + stride);
-            float acc[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-#pragma unroll
-            for (int u = 0; u < kTopk; ++u) {
-                if (r[u] < 0 || r[u] >= rows) continue;   // contributes nothing
-                const uint32_t words[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj[u], bf16lo(words[e])));
-                    acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj[u], bf16hi(words[e])));
+                v[u][0] = make_uint4(0u, 0u, 0u, 0u);
+                v[u][1] = make_uint4(0u, 0u, 0u, 0u);
+                if (r[u] >= 0 && r[u] < rows) {
+                    const uint4* row = reinterpret_cast<const uint4*>(y2 + r[u] * ld_y2);
+                    v[u][0] = __ldg(row + c);
+                    v[u][1] = __ldg(row + c + half);
+                } else if (c == 0) {
+                    record_error(status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
                 }
             }
-            uint32_t o[4];
+            fetch(i + stride);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
-                o[e] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int hh = 0; hh < 2; ++hh) {
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+                for (int u = 0; u < kTopk; ++u) {
+                    if (r[u] < 0 || r[u] >= rows) continue;   // contributes nothing
+                    const uint32_t words[4] = {v[u][hh].x, v[u][hh].y, v[u][hh].z, v[u][hh].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj[u], bf16lo(words[e])));
+                        acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj[u], bf16hi(words[e])));
+                    }
+                }
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+                    o[e] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                reinterpret_cast<uint4*>(out + t * ld_out)[c + hh * half] = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            reinterpret_cast<uint4*>(out + t * ld_out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
         }
         return;
     }
@@ -157,7 +171,7 @@ extern "C" nvfp4_status nvfp4_moe_combine(const void* y2, int64_t rows, int64_t 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t* src = static_cast<const uint16_t*>(y2);
     uint16_t* dst = static_cast<uint16_t*>(out);
-    if (topk == 8)
+    if (topk == 8 && chunks % 2 == 0)
         combine_kernel<8><<<grid, kCbThreads, 0, s>>>(src, rows, ld_y2, dst_rows, weights, tokens, topk, chunks,
                                                       dst, ld_out, ctx.status);
     else

@@ -48,7 +48,7 @@ def test_qwen3_moe_step_full(nv, orc):
     assert bad.size == 0, f"{len(bad)} differ, first {bad[:5].tolist()}"
 
 
-@pytest.mark.parametrize("T,K,H", [(37, 1, 64), (100, 3, 24), (513, 8, 2056)])
+@pytest.mark.parametrize("T,K,H", [(37, 1, 64), (100, 3, 24), (513, 8, 2056), (77, 8, 272), (5, 8, 16)])
 def test_small_shapes(nv, orc, T, K, H):
     rng = np.random.default_rng(T * K + H)
     R = 3 * T + 7
