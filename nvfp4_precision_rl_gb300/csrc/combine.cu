@@ -7,8 +7,8 @@
 // The reduction is binary32 in slot order, multiply then add, each one IEEE
 // operation (__fmul_rn / __fadd_rn: never contracted into an FMA), so the
 // result is bit-exact.  Memory-bound gather: one thread per (token, 8 columns)
-// -- with topk fixed at compile time (and an even number of 8-column chunks),
-// per (token, chunks c and c + chunks / 2) -- the topk 16-byte row loads
+// -- with topk fixed at compile time (an even number of 8-column chunks, and
+// enough of them), per (token, chunks c and c + chunks / 2) -- the topk 16-byte row loads
 // issued before any arithmetic; in the fixed-topk kernel the next item's rows
 // and weights are read while the current item's rows load, so each item waits
 // on one memory latency instead of two.
@@ -20,7 +20,7 @@ namespace {
 constexpr int kCbThreads = 256;
 constexpr int kCbMaxTopk = 32;
 
-template <int kTopk>   // 0: runtime topk
+template <int kTopk, int kPer>   // kTopk 0: runtime topk; kPer: 8-column chunks per item (1 or 2)
 __global__ void __launch_bounds__(kCbThreads) combine_kernel(const uint16_t* __restrict__ y2, int64_t rows,
                                                              int64_t ld_y2, const int32_t* __restrict__ dst,
                                                              const float* __restrict__ w, int64_t tokens,
@@ -30,9 +30,10 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(const uint16_t* __r
     const int64_t total = tokens * chunks;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if constexpr (kTopk > 0) {
-        // two chunks per item (c and c + chunks / 2 of one token): the next
-        // item's rows and weights are read while the current one's rows load
-        const int half = chunks >> 1;
+        // kPer chunks per item (c, and c + chunks / 2 when kPer is 2, of one
+        // token): the next item's rows and weights are read while the current
+        // one's rows load
+        const int half = chunks / kPer;
         const int64_t items = tokens * half;
         int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
         int32_t rn[kTopk];
@@ -56,22 +57,22 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(const uint16_t* __r
                 r[u] = rn[u];
                 wj[u] = wn[u];
             }
-            uint4 v[kTopk][2];
+            uint4 v[kTopk][kPer];
 #pragma unroll
             for (int u = 0; u < kTopk; ++u) {
-                v[u][0] = make_uint4(0u, 0u, 0u, 0u);
-                v[u][1] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int hh = 0; hh < kPer; ++hh) v[u][hh] = make_uint4(0u, 0u, 0u, 0u);
                 if (r[u] >= 0 && r[u] < rows) {
                     const uint4* row = reinterpret_cast<const uint4*>(y2 + r[u] * ld_y2);
-                    v[u][0] = __ldg(row + c);
-                    v[u][1] = __ldg(row + c + half);
+#pragma unroll
+                    for (int hh = 0; hh < kPer; ++hh) v[u][hh] = __ldg(row + c + hh * half);
                 } else if (c == 0) {
                     record_error(status, NVFP4_ERR_DEVICE_INPUT, DETAIL_GATHER_INDEX);
                 }
             }
             fetch(i + stride);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            for (int hh = 0; hh < kPer; ++hh) {
                 float acc[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -171,11 +172,17 @@ extern "C" nvfp4_status nvfp4_moe_combine(const void* y2, int64_t rows, int64_t 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t* src = static_cast<const uint16_t*>(y2);
     uint16_t* dst = static_cast<uint16_t*>(out);
-    if (topk == 8 && chunks % 2 == 0)
-        combine_kernel<8><<<grid, kCbThreads, 0, s>>>(src, rows, ld_y2, dst_rows, weights, tokens, topk, chunks,
-                                                      dst, ld_out, ctx.status);
+    // the two-chunk kernel holds 2 CTAs per SM; with fewer than ~8 of its items
+    // per resident thread the one-chunk kernel, with twice the CTAs, is faster
+    const bool two_chunks = chunks % 2 == 0 && total / 2 >= static_cast<int64_t>(ctx.sm_count) * 2 * kCbThreads * 8;
+    if (topk == 8 && two_chunks)
+        combine_kernel<8, 2><<<grid, kCbThreads, 0, s>>>(src, rows, ld_y2, dst_rows, weights, tokens, topk, chunks,
+                                                         dst, ld_out, ctx.status);
+    else if (topk == 8)
+        combine_kernel<8, 1><<<grid, kCbThreads, 0, s>>>(src, rows, ld_y2, dst_rows, weights, tokens, topk, chunks,
+                                                         dst, ld_out, ctx.status);
     else
-        combine_kernel<0><<<grid, kCbThreads, 0, s>>>(src, rows, ld_y2, dst_rows, weights, tokens, topk, chunks,
+        combine_kernel<0, 1><<<grid, kCbThreads, 0, s>>>(src, rows, ld_y2, dst_rows, weights, tokens, topk, chunks,
                                                       dst, ld_out, ctx.status);
     NVFP4_CHECK_LAUNCH();
     return NVFP4_OK;

@@ -48,8 +48,10 @@ def test_qwen3_moe_step_full(nv, orc):
     assert bad.size == 0, f"{len(bad)} differ, first {bad[:5].tolist()}"
 
 
-@pytest.mark.parametrize("T,K,H", [(37, 1, 64), (100, 3, 24), (513, 8, 2056), (77, 8, 272), (5, 8, 16)])
+@pytest.mark.parametrize("T,K,H", [(37, 1, 64), (100, 3, 24), (513, 8, 2056), (77, 8, 272), (5, 8, 16), (20000, 8, 512)])
 def test_small_shapes(nv, orc, T, K, H):
+    """Top-k weighted combine on random rows; (20000, 8, 512) has enough 8-column
+    chunk pairs for the two-chunk kernel on a 152-SM GPU."""
     rng = np.random.default_rng(T * K + H)
     R = 3 * T + 7
     y2 = W.to_bf16_bits(rng.standard_normal((R, H)).astype(np.float32))
