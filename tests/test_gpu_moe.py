@@ -21,7 +21,10 @@ def _ids(seed, T, E, k):
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 4, 1), (37, 8, 2), (300, 16, 4), (40, 64, 2),
-                                   (4096, 128, 8), (65536, 128, 8)])
+                                   (4096, 128, 8), (65536, 128, 8),
+                                   # 64 and 65 chunks of 1,024 ids: the two sides of the
+                                   # switch from the one-block scan to one block per expert
+                                   (8192, 128, 8), (8320, 128, 8), (8320, 1000, 8)])
 def test_permute_bit_exact(nv, orc, T, E, k):
     ids = _ids(T + E, T, E, k)
     got = nv.moe_permute(torch.from_numpy(ids).cuda(), E)
