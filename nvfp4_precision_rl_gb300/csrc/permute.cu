@@ -210,9 +210,11 @@ __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(const int32_
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kChunk;
     const int64_t c1 = min(c0 + kChunk, n);
+    int32_t e_next = (c0 + threadIdx.x < c1) ? ids[c0 + threadIdx.x] : -1;   // read a round ahead
     for (int64_t base = c0; base < c1; base += kPermThreads) {
         const int64_t i = base + threadIdx.x;
-        int32_t e = (i < c1) ? ids[i] : -1;
+        int32_t e = e_next;
+        e_next = (i + kPermThreads < c1) ? ids[i + kPermThreads] : -1;
         if (e >= E) e = -1;
         if (i < c1 && e < 0) dst_rows[i] = -1;   // dropped id (already reported by the count pass)
         const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
